@@ -1,0 +1,355 @@
+#!/usr/bin/env python
+"""Benchmark of the P-Cloth implicit-integration hot path on GB300.
+
+One "step" is one whole implicit step of the hot path through the C ABI
+(pcloth_step): per-step contact merge and assembly of A = M + h^2 sum K,
+b = h f; block-Jacobi PCG to |r| <= 1e-6 |b|; state update.  The default
+workload is the four-layer folded stack (4 x 455^2 vertices, 1,648,928
+triangles, ~82,810 fresh contacts per step, h = 5e-3), the synthetic stand-in
+for the pages' largest garment (1.65M triangles).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  The path does not shard: with N > 1 every
+rank runs an independent replica of the workload ("replicas only"), the
+barrier and the max over ranks of the timed region stay, and `value` counts
+the steps of all ranks.  `--impl reference` times the fp64 CPU oracle on the
+host cores on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "PCG iterations/s + implicit steps/s at 1.65M tris; SpMV GB/s vs HBM peak"
+UNIT = "implicit steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--config", default="C5", help="workload C1..C5 (default C5)")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--oracle-iters", type=int, default=8,
+                   help="oracle PCG iterations per reference sample step")
+    return p.parse_args()
+
+
+def workload_desc(w):
+    return dict(workload="%s: %s" % (w.name, w.description), vertices=w.n_verts,
+                triangles=w.triangles, springs=w.n_springs, contacts_per_step=w.max_contacts,
+                h=w.h, tol=w.tol, maxit=w.maxit)
+
+
+# ------------------------------------------------------------------ peaks --
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def stored_traffic(kernel_src_digest):
+    """DRAM bytes per launch of the PCG SpMV from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "spmv_pcg_C5_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_digest") == kernel_src_digest:
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def spmv_source_digest():
+    h = hashlib.sha256()
+    for f in ("spmv.cu", "pcloth_internal.cuh"):
+        with open(os.path.join(ROOT, "sparse_linear_solve_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- clocks --
+class Clocks:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(smax) if smax else None,
+                    power_w_max=max(power) if power else None,
+                    samples=len(sm), reasons=sorted(reasons))
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_sample(w, x, v, contacts, iters):
+    """Time the fp64 oracle on one bounded sample of a step: the full assembly
+    plus `iters` PCG iterations.  Returns (t_assembly, t_per_iteration)."""
+    from oracle import oracle
+    t0 = time.perf_counter()
+    s = oracle.assemble_workload(w, x, v, contacts)
+    t1 = time.perf_counter()
+    s.pcg(w.tol, iters)
+    t2 = time.perf_counter()
+    return t1 - t0, (t2 - t1) / max(iters, 1)
+
+
+def oracle_iterations_per_step(config, fallback):
+    """PCG iterations the oracle needs per step, from the committed table
+    written by oracle/iteration_table.py (fp64 oracle runs only)."""
+    path = os.path.join(ROOT, "oracle", "iteration_table.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        its = d[config]["iterations"]
+        return float(sum(its)) / len(its), "oracle table (%d steps)" % len(its)
+    except Exception:
+        return float(fallback), "GPU mean iteration count (oracle table absent)"
+
+
+# ------------------------------------------------------------------- arms --
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from sparse_linear_solve_gb300 import pcloth as pc
+    from sparse_linear_solve_gb300 import workloads as W
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.make(args.config)
+    K, Wm = args.steps, args.warmup
+    cloth = pc.PCloth.from_workload(w, device=dev)
+    x = torch.from_numpy(w.x0).to(dev)
+    v = torch.from_numpy(w.v0).to(dev)
+    dv = torch.empty_like(x)
+    host_contacts = [w.contacts(t) for t in range(Wm + K)]
+    dev_contacts = [pc.to_device_elements(c, dev) for c in host_contacts]
+    for t in range(Wm):
+        cloth.step(x, v, dev_contacts[t], w.h, w.tol, w.maxit, dv)
+    torch.cuda.synchronize()
+    nnzb_seen = []
+    cloth.profile(True)
+    cloth.profile_read(reset=True)
+    clocks = Clocks(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    its, codes = [], []
+    for t in range(K):
+        it, rr, code = cloth.step(x, v, dev_contacts[Wm + t], w.h, w.tol, w.maxit, dv)
+        its.append(it)
+        codes.append(code)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    prof = cloth.profile_read(reset=True)
+    nnzb_seen.append(cloth.nnzb())
+    cloth.profile(False)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- roofline of the dominant kernel: the PCG SpMV -------------------
+    n = w.n_verts
+    nnzb = nnzb_seen[-1]
+    bytes_per_launch = 40 * nnzb + 52 * n
+    launches = max(prof["spmv_launches"], 1)
+    spmv_avg_ms = prof["spmv_ms"] / launches
+    achieved = bytes_per_launch / (spmv_avg_ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    upd_bytes = 120 * n  # dv, p, r, q, P(36) read; dv, r, z written (bytes/vertex)
+    upd_avg_ms = prof["update_ms"] / max(prof["update_launches"], 1)
+
+    # ---- end to end through the host-buffer entry point ------------------
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(w.x0.copy()).pin_memory()
+        vh = torch.from_numpy(w.v0.copy()).pin_memory()
+        hc = []
+        for c in host_contacts:
+            if c.n:
+                hc.append(tuple(torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                                for a in (c.i, c.j, c.k, c.rest)))
+            else:
+                hc.append(None)
+        cloth.step_host(xh, vh, hc[0], w.h, w.tol, w.maxit)  # warm
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for t in range(K):
+            cloth.step_host(xh, vh, hc[Wm + t], w.h, w.tol, w.maxit)
+        t1 = time.perf_counter()
+        e_s = t1 - t0
+        if world > 1:
+            tt = torch.tensor([e_s], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_s = float(tt.item())
+        nc_mean = sum(c.n for c in host_contacts[Wm:]) / K
+        e2e = dict(value=world * K / e_s, unit=UNIT,
+                   h2d_bytes_per_step=int(2 * 12 * n + 16 * nc_mean),
+                   d2h_bytes_per_step=int(2 * 12 * n))
+
+    result = dict(
+        metric=METRIC, value=world * K / (ms * 1e-3), unit=UNIT, n_gpus=world, steps=K,
+        warmup=Wm, ms_per_step=ms / K, higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="f32 (fp32 storage/arithmetic, fp64 dot-product reductions)",
+        data="synthetic (seeded generator; no garment meshes available)",
+        config=dict(workload_desc(w), parallelism="replicas only (one independent cloth per GPU)",
+                    l2="inputs larger than L2: A is %.0f MB per step vs 129 MB L2" %
+                    (nnzb * 40 / 1e6)),
+        pcg_iterations_per_s=world * sum(its) / (ms * 1e-3),
+        pcg_iterations_per_s_solve_only=sum(its) / (prof["solve_ms"] * 1e-3),
+        pcg_iterations_mean=sum(its) / K,
+        assembly_ms=prof["assemble_ms"] / max(prof["assemble_calls"], 1),
+        spmv_gbs=achieved,
+        spmv_us=spmv_avg_ms * 1e3,
+        update_us=upd_avg_ms * 1e3,
+        update_gbs=upd_bytes / (upd_avg_ms * 1e-3) / 1e9 if upd_avg_ms > 0 else None,
+        codes=sorted(set(codes)),
+        roofline=dict(bound="hbm", kernel="spmv_tiles<true> (PCG SpMV, fused p update + p.q)",
+                      achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
+                      peak_source=peak_src, bytes_per_launch=bytes_per_launch,
+                      bytes_model="40 B/block (36 values + 4 colind) + 52 B/row (rowptr 4, "
+                                  "z 12, p_old 12 read; p 12, q 12 written)",
+                      traffic=stored_traffic(spmv_source_digest())),
+        clocks=clk,
+        gpu_launches=int(prof["kernel_launches"]),
+        e2e=e2e,
+    )
+
+    # ---- CPU baseline: the oracle on the host cores, bounded sample ------
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        c = host_contacts[Wm]
+        t_asm, t_it = oracle_sample(w, w.x0, w.v0, c if c.n else None, args.oracle_iters)
+        it_step, src = oracle_iterations_per_step(args.config, sum(its) / K)
+        step_s = t_asm + it_step * t_it
+        result["cpu_baseline"] = dict(
+            value=1.0 / step_s, unit=UNIT, cores=1, kind="oracle",
+            sample="fp64 C++ oracle, one thread: full assembly of one step (%.2f s) plus %d PCG "
+                   "iterations (%.3f s each), extrapolated to %.0f iterations per step (%s)"
+                   % (t_asm, args.oracle_iters, t_it, it_step, src))
+    cloth.close()
+    return result
+
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, same config, metric and unit."""
+    from sparse_linear_solve_gb300 import workloads as W
+    w = W.make(args.config)
+    K, Wm = args.steps, args.warmup
+    it_step, src = oracle_iterations_per_step(args.config, 1000)
+    samples = []
+    for t in range(Wm + K):
+        c = w.contacts(t)
+        iters = args.oracle_iters if t >= Wm else 1
+        t_asm, t_it = oracle_sample(w, w.x0, w.v0, c if c.n else None, iters)
+        if t >= Wm:
+            samples.append(t_asm + it_step * t_it)
+    step_s = sum(samples) / len(samples)
+    value = 1.0 / step_s
+    sample = ("fp64 C++ oracle, one thread: per step the full assembly plus %d PCG iterations, "
+              "extrapolated to %.0f iterations per step (%s)" % (args.oracle_iters, it_step, src))
+    return dict(metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=K, warmup=Wm,
+                ms_per_step=step_s * 1e3, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload_desc(w), parallelism="host, 1 thread"),
+                impl="reference",
+                cpu_baseline=dict(kind="oracle", cores=1, sample=sample, value=value, unit=UNIT),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,184 @@
+/*
+ * pcloth.h - C ABI of the GB300 implicit-integration hot path of P-Cloth.
+ *
+ * P-Cloth (arXiv 2008.00409, "P-Cloth: Interactive Complex Cloth Simulation on
+ * Multi-GPU Systems using Dynamic Matrix Assembly and Pipelined Implicit
+ * Integrators") integrates a cloth of p vertices with backward Euler
+ * (Sec. 2.5, Eq. (1)-(3)).  Each time step it
+ *
+ *   1. assembles the 3x3-block sparse system
+ *        A dv = b,   A = M + h^2 sum_e K_e,   b = h f(x_t + h v_t)
+ *      from every spring and contact element e = (i, j, k, L0) (Sec. 3.2,
+ *      "assembly elements"; Sec. 3.2.2, sparse matrix filling), with
+ *        K_e = k [ max(0, 1 - L0/l) (I - d d^T) + d d^T ]  at x_t,
+ *        F_e = k (l~ - L0) d~                             at x~ = x_t + h v_t,
+ *      K_e added to blocks (i,i), (j,j) and subtracted from (i,j), (j,i);
+ *      f_i = sum of element forces on i plus m_i g;
+ *   2. solves it by preconditioned conjugate gradients (Sec. 3.1 and the text
+ *      after Eq. (3)); the preconditioner here is block Jacobi (the inverse
+ *      of each 3x3 diagonal block), whose inner loop is the block sparse
+ *      matrix-vector product (Sec. 3.1, "the most computationally expensive
+ *      operator");
+ *   3. updates the state v += dv, x += h v.
+ *
+ * Storage (all on the device, owned by the library unless noted):
+ *   matrix     BSR3: rowptr int32[n+1], colind int32[nnzb] (sorted per row,
+ *              unique, diagonal always present), vals float32[nnzb][3][3]
+ *              (row-major blocks, rows consecutive);
+ *   vectors    float32[n][3] (x, y, z interleaved per vertex).
+ * The pattern of the springs is built once by pcloth_create; every
+ * pcloth_assemble merges that step's contact pairs into it in place, inside
+ * buffers sized at create for n + 2 * n_springs + 2 * max_contacts blocks, so
+ * no call after create allocates device memory.
+ *
+ * Streams: every call enqueues its work on the stream given at create (or by
+ * pcloth_set_stream) and returns without waiting, except where a call's
+ * comment says it synchronises.  Calls on one handle are not thread safe.
+ *
+ * Errors: every int-returning call returns PCLOTH_OK (0), PCLOTH_NOT_CONVERGED
+ * (1, results still valid) or a negative code.  Errors found by a kernel
+ * (bad index, capacity, non-finite value) are recorded in a device status
+ * word and reported by the next synchronising call (pcloth_solve,
+ * pcloth_step, pcloth_export, pcloth_nnzb, pcloth_sync); the status is then
+ * cleared.  pcloth_last_error returns a message for the last failure.
+ */
+#ifndef PCLOTH_H_
+#define PCLOTH_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  PCLOTH_OK = 0,
+  PCLOTH_NOT_CONVERGED = 1,    /* maxit reached; dv, iterations, residual valid */
+  PCLOTH_ERR_INVALID_ARG = -1, /* null/negative/out-of-order argument         */
+  PCLOTH_ERR_CAPACITY = -2,    /* more contacts than max_contacts, or sizes
+                                  beyond the int32 index range               */
+  PCLOTH_ERR_BAD_INDEX = -3,   /* element index outside [0, n) or i == j      */
+  PCLOTH_ERR_NONFINITE = -4,   /* NaN/Inf in x, v, the system or a residual,
+                                  or a zero-length element                   */
+  PCLOTH_ERR_BREAKDOWN = -5,   /* PCG: p.Ap <= 0 or r.z < 0 (not SPD)         */
+  PCLOTH_ERR_CUDA = -6,        /* a CUDA runtime call failed                  */
+  PCLOTH_ERR_STATE = -7        /* call out of order (solve before assemble)   */
+};
+
+typedef struct pcloth* pcloth_t; /* opaque handle, owned by the library */
+
+/* The cloth: n_verts vertices with masses (device pointer, float32[n_verts],
+ * kg) and a uniform gravity acceleration (m/s^2, e.g. {0, 0, -9.8}).
+ * Sec. 2.5: M is the (block-diagonal) mass matrix of Eq. (1). */
+typedef struct {
+  int32_t n_verts;
+  const float* mass;
+  float gravity[3];
+} pcloth_mesh;
+
+/* A list of n elements (springs or contacts), device pointers:
+ * i, j int32[n] vertex indices (i != j, both in [0, n_verts)), k float32[n]
+ * stiffness (N/m), rest float32[n] rest length (m).  Sec. 3.2: the
+ * "assembly elements" that form f and J of Eq. (3); contacts are penalty
+ * springs of the same law.  Duplicated pairs are summed into one block. */
+typedef struct {
+  int32_t n;
+  const int32_t* i;
+  const int32_t* j;
+  const float* k;
+  const float* rest;
+} pcloth_springs;
+
+/* Options: max_contacts sizes the per-step contact buffers; device is the
+ * CUDA device ordinal; stream is a cudaStream_t (0 = the legacy default
+ * stream).  max_iter_chunk: PCG iterations enqueued between convergence
+ * polls (0 = default 16). */
+typedef struct {
+  int32_t max_contacts;
+  int device;
+  void* stream;
+  int32_t max_iter_chunk;
+} pcloth_opts;
+
+/* Create a handle for a cloth and its (static) springs.  Copies the springs
+ * to the host once, validates them (PCLOTH_ERR_BAD_INDEX on a bad index),
+ * builds the static block pattern (Sec. 3.2.2 steps 1-3: diagonal plus both
+ * directions of every spring, sorted, duplicates merged) and allocates every
+ * device buffer at its capacity.  Synchronises.  On failure *out is NULL. */
+int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* springs,
+                  const pcloth_opts* opts, pcloth_t* out);
+
+/* Assemble the step's system at state (x, v) (device float32[n][3]) with
+ * time step h and this step's contacts (may be NULL or n = 0): evaluates
+ * every element (K_e at x, F_e at x + h v), merges the contact pairs into the
+ * pattern (key sort, rows rebuilt in place), fills the block values
+ * A = M + h^2 sum K_e, the right-hand side b = h f and the block-Jacobi
+ * inverses.  Sec. 2.5 Eq. (3); Sec. 3.2.2 steps 1-5.  Asynchronous;
+ * PCLOTH_ERR_CAPACITY if contacts->n > max_contacts (checked on the host). */
+int pcloth_assemble(pcloth_t h, const float* x, const float* v,
+                    const pcloth_springs* contacts, float dt);
+
+/* out = A in for the last assembled A (device float32[n][3] each; in and
+ * out must not overlap).  Sec. 3.1 (SpMV).  Asynchronous. */
+int pcloth_spmv(pcloth_t h, const float* in, float* out);
+
+/* Solve A dv = b by block-Jacobi PCG from dv = 0 until
+ * |r|_2 <= tol |b|_2 (recursive residual) or maxit iterations; dv is device
+ * float32[n][3]; *iterations and *rel_residual (= |r|/|b|) are written on
+ * the host.  Sec. 3.1 / Eq. (3).  Synchronises at the end (and polls the
+ * device every max_iter_chunk iterations without stalling it). */
+int pcloth_solve(pcloth_t h, double tol, int32_t maxit, float* dv,
+                 int32_t* iterations, double* rel_residual);
+
+/* One whole implicit step: assemble at (x, v), solve, then update the state
+ * in place: v += dv, x += dt v (Eq. (3) with backward Euler).  x, v device
+ * float32[n][3]; dv may be NULL (library scratch is used).  Synchronises. */
+int pcloth_step(pcloth_t h, float* x, float* v, const pcloth_springs* contacts,
+                float dt, double tol, int32_t maxit, float* dv,
+                int32_t* iterations, double* rel_residual);
+
+/* pcloth_step with HOST buffers: x, v are host float32[n][3] (pinned memory
+ * recommended), contacts' pointers are host arrays.  Copies the inputs to
+ * library-owned device buffers, runs the step and copies x, v back.
+ * Synchronises. */
+int pcloth_step_host(pcloth_t h, float* x, float* v,
+                     const pcloth_springs* contacts, float dt, double tol,
+                     int32_t maxit, int32_t* iterations, double* rel_residual);
+
+/* Number of blocks of the last assembled matrix (synchronises). */
+int pcloth_nnzb(pcloth_t h, int64_t* nnzb);
+
+/* Copy the last assembled system into caller-owned device buffers (any may
+ * be NULL): rowptr int32[n+1], colind int32[nnzb], vals float32[nnzb*9],
+ * b float32[n*3], pinv float32[n*9].  Synchronises. */
+int pcloth_export(pcloth_t h, int32_t* rowptr, int32_t* colind, float* vals,
+                  float* b, float* pinv);
+
+/* Replace the stream used by later calls. */
+int pcloth_set_stream(pcloth_t h, void* stream);
+
+/* Wait for the handle's stream and report any device-side error. */
+int pcloth_sync(pcloth_t h);
+
+/* Message for the last error on this handle ("" if none); NULL handle gives
+ * the message of the last failed pcloth_create. */
+const char* pcloth_last_error(pcloth_t h);
+
+/* Profiling: while enabled, the library records CUDA events on its stream
+ * around every assembly, SpMV and PCG-update launch and accumulates their
+ * device time.  pcloth_profile_read fills ms_out[4] = {assembly, PCG SpMV,
+ * PCG update, whole solves} in milliseconds and counts_out[6] =
+ * {assemblies, SpMV launches, update launches, solves, PCG iterations,
+ * kernels launched by this handle}; reset != 0 zeroes the accumulators. */
+int pcloth_profile_enable(pcloth_t h, int on);
+int pcloth_profile_read(pcloth_t h, double* ms_out, int64_t* counts_out,
+                        int reset);
+
+/* Free every buffer of the handle (synchronises its stream first). */
+void pcloth_destroy(pcloth_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PCLOTH_H_ */

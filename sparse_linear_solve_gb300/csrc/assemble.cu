@@ -1,0 +1,529 @@
+// Per-step assembly of A dv = b (P-Cloth, arXiv 2008.00409: Sec. 2.5
+// Eq. (3) for the system, Sec. 3.2 for the assembly elements, Sec. 3.2.2 for
+// the sparse matrix filling).
+//
+// The page fills an ELL index table with atomics, sorts and compacts each row
+// with one thread per row, then fills values with atomics.  This design keeps
+// BSR3 and replaces those steps with deterministic ones:
+//
+//   contact_keys     two directed keys (row << B | col) per contact
+//   radix sort       stable, so equal keys keep their input order
+//   contact_classify flag the first entry of every (row, col) pair that is
+//                    not already a block of the static spring pattern
+//   scan + compact   list of new blocks, sorted by (row, col)
+//   tile_bounds      per tile of rows: first new block / first entry
+//   assemble_rows    per tile: rebuild rowptr and colind in place (static
+//                    blocks shifted by the new blocks of earlier rows, new
+//                    blocks merged into their rows), evaluate every element
+//                    of every off-diagonal block, reduce each row into its
+//                    diagonal block, b = h f and the block-Jacobi inverse.
+//
+// No float atomics: every sum has a fixed order, so the assembled system is
+// bitwise reproducible.  Each off-diagonal block is computed by its own row;
+// the block (j, i) is computed from the negated edge vector and is therefore
+// bitwise equal to the block (i, j).
+
+#include "pcloth_internal.cuh"
+
+namespace pcloth_impl {
+namespace {
+
+constexpr uint64_t kSentinel = ~0ull;
+
+struct AsmArgs {
+  int32_t n;
+  int B;                 // bits per index in a key
+  float dt, h2;
+  float gx, gy, gz;
+  const float* x;
+  const float* v;
+  const float* mass;
+  const int32_t* rowptr_s;
+  const int32_t* colind_s;
+  const int32_t* sblk_ptr;
+  const float2* sentry;
+  int has_contacts;
+  const uint64_t* skey;    // sorted contact keys
+  const int32_t* sval;     // contact id of each sorted key
+  const float* ck;
+  const float* cr;
+  const uint64_t* newkey;
+  const int32_t* newfirst;
+  const int32_t* tile_nb;
+  const int32_t* tile_eb;
+  const int32_t* counters;  // [0] new blocks, [1] valid entries
+  int32_t* rowptr;
+  int32_t* colind;
+  float* vals;
+  float* rhs;
+  float* pinv;
+  uint32_t* status;
+};
+
+__global__ void contact_keys(int32_t nc, int32_t n, int B, const int32_t* __restrict__ ci,
+                             const int32_t* __restrict__ cj, const float* __restrict__ ck,
+                             const float* __restrict__ cr, uint64_t* __restrict__ keys,
+                             int32_t* __restrict__ vals, uint32_t* status) {
+  const int32_t c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= nc) return;
+  const int32_t i = ci[c], j = cj[c];
+  const bool ok = i >= 0 && i < n && j >= 0 && j < n && i != j;
+  if (!ok) atomicOr(status, ST_BAD_INDEX);
+  if (!isfinite(ck[c]) || !isfinite(cr[c])) atomicOr(status, ST_NONFINITE);
+  keys[2 * int64_t(c)] = ok ? (uint64_t(i) << B) | uint64_t(j) : kSentinel;
+  keys[2 * int64_t(c) + 1] = ok ? (uint64_t(j) << B) | uint64_t(i) : kSentinel;
+  vals[2 * int64_t(c)] = c;
+  vals[2 * int64_t(c) + 1] = c;
+}
+
+__device__ __forceinline__ bool static_has(const int32_t* __restrict__ colind_s,
+                                           int32_t lo, int32_t hi, int32_t col) {
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    const int32_t c = colind_s[mid];
+    if (c == col) return true;
+    if (c < col) lo = mid + 1; else hi = mid;
+  }
+  return false;
+}
+
+__global__ void contact_classify(int32_t m, int B, const uint64_t* __restrict__ skey,
+                                 const int32_t* __restrict__ rowptr_s,
+                                 const int32_t* __restrict__ colind_s,
+                                 int32_t* __restrict__ flags, int32_t* __restrict__ counters) {
+  const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= m) return;
+  const uint64_t key = skey[t];
+  int32_t f = 0;
+  if (key != kSentinel) {
+    const uint64_t mask = (uint64_t(1) << B) - 1;
+    const int32_t row = int32_t(key >> B), col = int32_t(key & mask);
+    const bool first = (t == 0) || skey[t - 1] != key;
+    if (first && !static_has(colind_s, rowptr_s[row], rowptr_s[row + 1], col)) f = 1;
+    // sentinels sort last: the last valid entry records the valid count
+    if (t + 1 == m || skey[t + 1] == kSentinel) counters[1] = t + 1;
+  }
+  flags[t] = f;
+}
+
+__global__ void contact_compact(int32_t m, const uint64_t* __restrict__ skey,
+                                const int32_t* __restrict__ prefix,
+                                const int32_t* __restrict__ counters,
+                                uint64_t* __restrict__ newkey, int32_t* __restrict__ newfirst) {
+  const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= m) return;
+  const int32_t next = (t + 1 < m) ? prefix[t + 1] : counters[0];
+  if (next != prefix[t]) {
+    newkey[prefix[t]] = skey[t];
+    newfirst[prefix[t]] = t;
+  }
+}
+
+__device__ __forceinline__ int32_t lower_bound_key(const uint64_t* __restrict__ a,
+                                                   int32_t lo, int32_t hi, uint64_t key) {
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (a[mid] < key) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void tile_bounds(int32_t ntiles, int32_t n, int B, int has_contacts,
+                            const uint64_t* __restrict__ newkey,
+                            const uint64_t* __restrict__ skey,
+                            const int32_t* __restrict__ counters,
+                            int32_t* __restrict__ tile_nb, int32_t* __restrict__ tile_eb) {
+  const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t > ntiles) return;
+  if (!has_contacts) {
+    tile_nb[t] = 0;
+    tile_eb[t] = 0;
+    return;
+  }
+  const int64_t r = min(int64_t(t) * kAsmRows, int64_t(n));
+  const uint64_t key = uint64_t(r) << B;
+  tile_nb[t] = lower_bound_key(newkey, 0, counters[0], key);
+  tile_eb[t] = lower_bound_key(skey, 0, counters[1], key);
+}
+
+// Length minus rest length, l - L0 = (|e|^2 - L0^2) / (l + L0), with the
+// squares summed in fp64 (exact for fp32 components).  Near the rest length
+// the plain fp32 difference l - L0 is pure rounding noise (~1e-7 L0); that
+// noise would give a spring at rest a spurious transverse stiffness
+// k (1 - L0/l) (I - d d^T) along exactly the soft out-of-plane directions of
+// a flat sheet, whose only other stiffness is the mass term.
+__device__ __forceinline__ float stretch_of(float3 e, float l, float L0) {
+  const double d2 = double(e.x) * e.x + double(e.y) * e.y + double(e.z) * e.z -
+                    double(L0) * L0;
+  return float(d2) / (l + L0);
+}
+
+// K (6 unique entries of the symmetric 3x3 block) and F of one element seen
+// from vertex i: K at x, force at x~ = x + h v.  e = x_j - x_i is passed in
+// (it is shared by all elements of a block) and w = v_j - v_i.  The advanced
+// edge is formed as e + h w, not as a difference of advanced positions, so
+// it keeps the accuracy of the short edge instead of that of the (possibly
+// metres-large) coordinates; both l - L0 and l~ - L0 come from stretch_of.
+__device__ __forceinline__ void element_terms(float3 e, float3 w, float dt, float k, float L0,
+                                              float (&K)[6], float (&F)[3]) {
+  const float l = sqrtf(e.x * e.x + e.y * e.y + e.z * e.z);
+  const float inv = 1.0f / l;
+  const float dx = e.x * inv, dy = e.y * inv, dz = e.z * inv;
+  const float tension = fmaxf(0.0f, stretch_of(e, l, L0) * inv);   // max(0, 1 - L0/l)
+  const float a = k * tension;        // k * max(0, 1 - L0/l)
+  const float c = k - a;              // k * (1 - max(...))
+  K[0] += a + c * dx * dx;
+  K[1] += c * dx * dy;
+  K[2] += c * dx * dz;
+  K[3] += a + c * dy * dy;
+  K[4] += c * dy * dz;
+  K[5] += a + c * dz * dz;
+  const float3 f = make_float3(fmaf(dt, w.x, e.x), fmaf(dt, w.y, e.y), fmaf(dt, w.z, e.z));
+  const float fx = f.x, fy = f.y, fz = f.z;
+  const float lt = sqrtf(fx * fx + fy * fy + fz * fz);
+  const float stretch = stretch_of(f, lt, L0);   // l~ - L0
+  const float s = k * stretch / lt;
+  F[0] += s * fx;
+  F[1] += s * fy;
+  F[2] += s * fz;
+}
+
+__device__ __forceinline__ float3 ld3(const float* p, int64_t i) {
+  return make_float3(p[3 * i], p[3 * i + 1], p[3 * i + 2]);
+}
+
+// Merge position p of two sorted disjoint lists S (static cols) and T (new
+// contact cols): returns a = number of S entries before position p.
+__device__ __forceinline__ int32_t merge_split(const int32_t* __restrict__ S, int32_t nS,
+                                               const uint64_t* __restrict__ T, int32_t nT,
+                                               uint64_t mask, int32_t p) {
+  int32_t lo = max(0, p - nT), hi = min(p, nS);
+  while (lo < hi) {
+    const int32_t mid = (lo + hi + 1) >> 1;
+    if (S[mid - 1] < int32_t(T[p - mid] & mask)) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct RowInfo {
+  int32_t sb, se;   // static slots
+  int32_t nb, ne;   // new blocks
+  int32_t eb, ee;   // sorted contact entries
+  int32_t ob;       // first output block
+};
+
+// Computes block `o` (absolute output index) of tile-local row `ri`; writes
+// the value (9 floats, -h^2 K sum) and the force sum into shared staging.
+__device__ __forceinline__ void compute_block(const AsmArgs& a, int32_t i, const RowInfo& R,
+                                              int32_t p, float* __restrict__ stv,
+                                              float* __restrict__ stf, int32_t* __restrict__ stc,
+                                              int32_t m_valid) {
+  const uint64_t mask = (uint64_t(1) << a.B) - 1;
+  const int32_t nS = R.se - R.sb, nT = R.ne - R.nb;
+  int32_t col, sslot = -1, nk = -1;
+  if (nT == 0) {
+    sslot = R.sb + p;
+    col = a.colind_s[sslot];
+  } else {
+    const int32_t s = merge_split(a.colind_s + R.sb, nS, a.newkey + R.nb, nT, mask, p);
+    const int32_t t = p - s;
+    if (s < nS && (t >= nT || a.colind_s[R.sb + s] < int32_t(a.newkey[R.nb + t] & mask))) {
+      sslot = R.sb + s;
+      col = a.colind_s[sslot];
+    } else {
+      nk = R.nb + t;
+      col = int32_t(a.newkey[nk] & mask);
+    }
+  }
+  float K[6] = {0, 0, 0, 0, 0, 0}, F[3] = {0, 0, 0};
+  if (col != i) {
+    const float3 xi = ld3(a.x, i), vi = ld3(a.v, i);
+    const float3 xj = ld3(a.x, col), vj = ld3(a.v, col);
+    const float3 ed = make_float3(xj.x - xi.x, xj.y - xi.y, xj.z - xi.z);
+    const float3 wd = make_float3(vj.x - vi.x, vj.y - vi.y, vj.z - vi.z);
+    if (sslot >= 0) {
+      const int32_t e1 = a.sblk_ptr[sslot + 1];
+      for (int32_t e = a.sblk_ptr[sslot]; e < e1; ++e) {
+        const float2 kl = a.sentry[e];
+        element_terms(ed, wd, a.dt, kl.x, kl.y, K, F);
+      }
+    }
+    // contacts on this (row, col) pair: a run of equal sorted keys
+    int32_t t0 = -1;
+    const uint64_t key = (uint64_t(i) << a.B) | uint64_t(col);
+    if (nk >= 0) {
+      t0 = a.newfirst[nk];
+    } else if (R.ee > R.eb) {
+      const int32_t t = lower_bound_key(a.skey, R.eb, R.ee, key);
+      if (t < R.ee && a.skey[t] == key) t0 = t;
+    }
+    if (t0 >= 0) {
+      for (int32_t t = t0; t < m_valid && a.skey[t] == key; ++t) {
+        const int32_t c = a.sval[t];
+        element_terms(ed, wd, a.dt, a.ck[c], a.cr[c], K, F);
+      }
+    }
+  }
+  const float h2 = a.h2;
+  stv[0] = -h2 * K[0]; stv[1] = -h2 * K[1]; stv[2] = -h2 * K[2];
+  stv[3] = -h2 * K[1]; stv[4] = -h2 * K[3]; stv[5] = -h2 * K[4];
+  stv[6] = -h2 * K[2]; stv[7] = -h2 * K[4]; stv[8] = -h2 * K[5];
+  stf[0] = F[0]; stf[1] = F[1]; stf[2] = F[2];
+  *stc = col;
+}
+
+// Diagonal block, right-hand side and block-Jacobi inverse of row i from the
+// accumulated off-diagonal sums (Ks = h^2 sum K, 6 unique entries) and force.
+__device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const float (&Ks)[6],
+                                           const float (&Fs)[3], float* __restrict__ D) {
+  const float m = a.mass[i];
+  D[0] = m + Ks[0]; D[1] = Ks[1]; D[2] = Ks[2];
+  D[3] = Ks[1]; D[4] = m + Ks[3]; D[5] = Ks[4];
+  D[6] = Ks[2]; D[7] = Ks[4]; D[8] = m + Ks[5];
+  const float b0 = a.dt * (Fs[0] + m * a.gx);
+  const float b1 = a.dt * (Fs[1] + m * a.gy);
+  const float b2 = a.dt * (Fs[2] + m * a.gz);
+  a.rhs[3 * int64_t(i)] = b0;
+  a.rhs[3 * int64_t(i) + 1] = b1;
+  a.rhs[3 * int64_t(i) + 2] = b2;
+  // inverse of the symmetric block by its adjugate
+  const float c00 = D[4] * D[8] - D[5] * D[7];
+  const float c01 = D[5] * D[6] - D[3] * D[8];
+  const float c02 = D[3] * D[7] - D[4] * D[6];
+  const float c11 = D[0] * D[8] - D[2] * D[6];
+  const float c12 = D[2] * D[3] - D[0] * D[5];
+  const float c22 = D[0] * D[4] - D[1] * D[3];
+  const float det = D[0] * c00 + D[1] * c01 + D[2] * c02;
+  const float id = 1.0f / det;
+  float* P = a.pinv + 9 * int64_t(i);
+  P[0] = c00 * id; P[1] = c01 * id; P[2] = c02 * id;
+  P[3] = c01 * id; P[4] = c11 * id; P[5] = c12 * id;
+  P[6] = c02 * id; P[7] = c12 * id; P[8] = c22 * id;
+  bool ok = finite3(b0, b1, b2) && isfinite(det) && det > 0.0f;
+#pragma unroll
+  for (int t = 0; t < 9; ++t) ok = ok && isfinite(D[t]);
+  if (!ok) atomicOr(a.status, ST_NONFINITE);
+}
+
+__global__ void __launch_bounds__(kAsmThreads)
+assemble_rows(AsmArgs a) {
+  __shared__ RowInfo rows[kAsmRows + 1];
+  __shared__ float stv[kAsmCap * 9];
+  __shared__ float stf[kAsmCap * 3];
+  __shared__ int32_t stc[kAsmCap];
+  __shared__ float red[9][kAsmThreads / 32];
+  __shared__ float acc[9];
+
+  const int32_t r0 = blockIdx.x * kAsmRows;
+  const int32_t nrows = min(kAsmRows, a.n - r0);
+  const int32_t m_valid = a.has_contacts ? a.counters[1] : 0;
+  const uint64_t mask = (uint64_t(1) << a.B) - 1;
+  (void)mask;
+
+  // ---- phase 1: row bounds, rebuilt row pointers ------------------------
+  if (threadIdx.x <= nrows) {
+    const int32_t ri = threadIdx.x, i = r0 + ri;
+    RowInfo R;
+    R.sb = a.rowptr_s[i];
+    R.se = (ri < nrows) ? a.rowptr_s[i + 1] : R.sb;
+    if (a.has_contacts) {
+      const int32_t nb0 = a.tile_nb[blockIdx.x], nb1 = a.tile_nb[blockIdx.x + 1];
+      const int32_t eb0 = a.tile_eb[blockIdx.x], eb1 = a.tile_eb[blockIdx.x + 1];
+      const uint64_t key = uint64_t(i) << a.B;
+      R.nb = (ri == 0) ? nb0 : (ri == nrows ? nb1 : lower_bound_key(a.newkey, nb0, nb1, key));
+      R.eb = (ri == 0) ? eb0 : (ri == nrows ? eb1 : lower_bound_key(a.skey, eb0, eb1, key));
+    } else {
+      R.nb = 0;
+      R.eb = 0;
+    }
+    R.ob = R.sb + R.nb;
+    rows[ri] = R;
+    if (ri < nrows || i == a.n) a.rowptr[i] = R.ob;
+  }
+  __syncthreads();
+  if (threadIdx.x < nrows) {
+    rows[threadIdx.x].ne = rows[threadIdx.x + 1].nb;
+    rows[threadIdx.x].ee = rows[threadIdx.x + 1].eb;
+  }
+  __syncthreads();
+
+  // ---- phase 2..4: groups of whole rows that fit in the staging ---------
+  int32_t g = 0;
+  while (g < nrows) {
+    int32_t e = g + 1;
+    while (e < nrows && rows[e + 1].ob - rows[g].ob <= kAsmCap) ++e;
+    const int32_t gob = rows[g].ob;
+    const int32_t nblk = rows[e].ob - gob;
+    if (nblk <= kAsmCap) {
+      // phase 2: every block of the group, one thread per block
+      for (int32_t o = threadIdx.x; o < nblk; o += kAsmThreads) {
+        // row of block o: last ri in [g, e) with rows[ri].ob <= gob + o
+        int32_t lo = g, hi = e - 1;
+        while (lo < hi) {
+          const int32_t mid = (lo + hi + 1) >> 1;
+          if (rows[mid].ob <= gob + o) lo = mid; else hi = mid - 1;
+        }
+        const RowInfo R = rows[lo];
+        compute_block(a, r0 + lo, R, gob + o - R.ob, &stv[9 * o], &stf[3 * o], &stc[o], m_valid);
+      }
+      __syncthreads();
+      // phase 3: one thread per row reduces its blocks into the diagonal
+      for (int32_t ri = g + threadIdx.x; ri < e; ri += kAsmThreads) {
+        const int32_t i = r0 + ri;
+        const int32_t o0 = rows[ri].ob - gob, o1 = rows[ri + 1].ob - gob;
+        float Ks[6] = {0, 0, 0, 0, 0, 0}, Fs[3] = {0, 0, 0};
+        int32_t dpos = -1;
+        for (int32_t o = o0; o < o1; ++o) {
+          if (stc[o] == i) { dpos = o; continue; }
+          const float* s = &stv[9 * o];
+          Ks[0] -= s[0]; Ks[1] -= s[1]; Ks[2] -= s[2];
+          Ks[3] -= s[4]; Ks[4] -= s[5]; Ks[5] -= s[8];
+          Fs[0] += stf[3 * o]; Fs[1] += stf[3 * o + 1]; Fs[2] += stf[3 * o + 2];
+        }
+        float D[9];
+        finish_row(a, i, Ks, Fs, D);
+        if (dpos >= 0) {
+#pragma unroll
+          for (int t = 0; t < 9; ++t) stv[9 * dpos + t] = D[t];
+        } else {
+          atomicOr(a.status, ST_CAPACITY);  // diagonal missing: cannot happen
+        }
+      }
+      __syncthreads();
+      // phase 4: coalesced write-out of values and column indices
+      float* dst = a.vals + 9 * int64_t(gob);
+      for (int32_t f = threadIdx.x; f < 9 * nblk; f += kAsmThreads) dst[f] = stv[f];
+      for (int32_t o = threadIdx.x; o < nblk; o += kAsmThreads) a.colind[gob + o] = stc[o];
+      __syncthreads();
+    } else {
+      // one row longer than the staging: stream it through in pieces
+      const int32_t ri = g, i = r0 + ri;
+      const RowInfo R = rows[ri];
+      if (threadIdx.x < 9) acc[threadIdx.x] = 0.f;
+      int32_t dpos_abs = -1;
+      for (int32_t c0 = 0; c0 < nblk; c0 += kAsmCap) {
+        const int32_t cn = min(kAsmCap, nblk - c0);
+        __syncthreads();
+        for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads)
+          compute_block(a, i, R, c0 + o, &stv[9 * o], &stf[3 * o], &stc[o], m_valid);
+        __syncthreads();
+        // fixed-order partial sums: thread t owns blocks t, t+T, ...
+        float part[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+        for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads) {
+          if (stc[o] == i) { dpos_abs = gob + c0 + o; continue; }
+          const float* s = &stv[9 * o];
+          part[0] -= s[0]; part[1] -= s[1]; part[2] -= s[2];
+          part[3] -= s[4]; part[4] -= s[5]; part[5] -= s[8];
+          part[6] += stf[3 * o]; part[7] += stf[3 * o + 1]; part[8] += stf[3 * o + 2];
+        }
+#pragma unroll
+        for (int q = 0; q < 9; ++q) {
+          float vq = part[q];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) vq += __shfl_down_sync(0xffffffffu, vq, off);
+          if ((threadIdx.x & 31) == 0) red[q][threadIdx.x >> 5] = vq;
+        }
+        __syncthreads();
+        if (threadIdx.x < 9) {
+          float s = 0.f;
+          for (int w = 0; w < kAsmThreads / 32; ++w) s += red[threadIdx.x][w];
+          acc[threadIdx.x] += s;
+        }
+        float* dst = a.vals + 9 * (int64_t(gob) + c0);
+        for (int32_t f = threadIdx.x; f < 9 * cn; f += kAsmThreads) dst[f] = stv[f];
+        for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads) a.colind[gob + c0 + o] = stc[o];
+      }
+      __syncthreads();
+      // the thread that saw the diagonal writes it (exactly one does)
+      if (dpos_abs >= 0) {
+        const float Ks[6] = {acc[0], acc[1], acc[2], acc[3], acc[4], acc[5]};
+        const float Fs[3] = {acc[6], acc[7], acc[8]};
+        float D[9];
+        finish_row(a, i, Ks, Fs, D);
+        float* dst = a.vals + 9 * int64_t(dpos_abs);
+#pragma unroll
+        for (int t = 0; t < 9; ++t) dst[t] = D[t];
+      }
+      __syncthreads();
+    }
+    g = e;
+  }
+}
+
+}  // namespace
+
+int assemble_system(Handle* h, const float* x, const float* v,
+                    const pcloth_springs* contacts, float dt) {
+  const int32_t nc = contacts ? contacts->n : 0;
+  const int B = h->key_bits;
+  const int32_t ntiles = (h->n + kAsmRows - 1) / kAsmRows;
+  cudaStream_t s = h->stream;
+  if (h->prof.on) cudaEventRecord(h->ev[0], s);
+  int rc = PCLOTH_OK;
+  AsmArgs a{};
+  a.has_contacts = nc > 0;
+  if (nc > 0) {
+    const int32_t m = 2 * nc;
+    contact_keys<<<(nc + 255) / 256, 256, 0, s>>>(nc, h->n, B, contacts->i, contacts->j,
+                                                   contacts->k, contacts->rest, h->ckey[0],
+                                                   h->cval[0], h->d_status);
+    cudaMemsetAsync(h->counters, 0, 4 * sizeof(int32_t), s);
+    h->launches += 1;
+    int cur = radix_sort_pairs(h, h->ckey, h->cval, m, 2 * B);
+    if (cur < 0) return cur;
+    contact_classify<<<(m + 255) / 256, 256, 0, s>>>(m, B, h->ckey[cur], h->rowptr_s,
+                                                     h->colind_s, h->flags, h->counters);
+    h->launches += 1;
+    rc = scan_exclusive(h, h->flags, m, h->counters);
+    if (rc != PCLOTH_OK) return rc;
+    contact_compact<<<(m + 255) / 256, 256, 0, s>>>(m, h->ckey[cur], h->flags, h->counters,
+                                                    h->newkey, h->newfirst);
+    h->launches += 1;
+    a.skey = h->ckey[cur];
+    a.sval = h->cval[cur];
+    a.ck = contacts->k;
+    a.cr = contacts->rest;
+  }
+  tile_bounds<<<(ntiles + 1 + 255) / 256, 256, 0, s>>>(ntiles, h->n, B, nc > 0, h->newkey,
+                                                        a.skey, h->counters, h->tile_nb,
+                                                        h->tile_eb);
+  h->launches += 1;
+  a.n = h->n;
+  a.B = B;
+  a.dt = dt;
+  a.h2 = dt * dt;
+  a.gx = h->gravity[0];
+  a.gy = h->gravity[1];
+  a.gz = h->gravity[2];
+  a.x = x;
+  a.v = v;
+  a.mass = h->mass;
+  a.rowptr_s = h->rowptr_s;
+  a.colind_s = h->colind_s;
+  a.sblk_ptr = h->sblk_ptr;
+  a.sentry = h->sentry;
+  a.newkey = h->newkey;
+  a.newfirst = h->newfirst;
+  a.tile_nb = h->tile_nb;
+  a.tile_eb = h->tile_eb;
+  a.counters = h->counters;
+  a.rowptr = h->rowptr;
+  a.colind = h->colind;
+  a.vals = h->vals;
+  a.rhs = h->rhs;
+  a.pinv = h->pinv;
+  a.status = h->d_status;
+  assemble_rows<<<ntiles, kAsmThreads, 0, s>>>(a);
+  h->launches += 1;
+  if (h->prof.on) {
+    cudaEventRecord(h->ev[1], s);
+    cudaEventSynchronize(h->ev[1]);
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, h->ev[0], h->ev[1]);
+    h->prof.assemble_ms += ms;
+    h->prof.assemble_calls += 1;
+  }
+  return check_launch(h, "assembly");
+}
+
+}  // namespace pcloth_impl

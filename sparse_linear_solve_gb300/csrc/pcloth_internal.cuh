@@ -1,0 +1,211 @@
+// Internal declarations shared by the CUDA sources of libpcloth.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "pcloth.h"
+
+namespace pcloth_impl {
+
+// ---------------------------------------------------------------- status --
+// Device-side error bits (ORed into Handle::d_status by kernels).
+enum : uint32_t {
+  ST_BAD_INDEX = 1u << 0,
+  ST_NONFINITE = 1u << 1,
+  ST_BREAKDOWN = 1u << 2,
+  ST_CAPACITY = 1u << 3,
+  ST_WAIT_TIMEOUT = 1u << 4,   // a bounded device wait gave up
+};
+
+// Device state of one PCG solve (written by kernels, read by the host).
+struct PcgState {
+  int32_t done;        // 1 once converged, broken down or non-finite
+  int32_t iterations;  // iterations completed when done was set
+  int32_t code;        // PCLOTH_OK / _NOT_CONVERGED / _ERR_*
+  int32_t pad;
+  double relres;       // |r| / |b| at stop
+  double bnorm;        // |b|
+};
+
+// ------------------------------------------------------------ sizes --------
+constexpr int kSortBits = 8;                 // radix digit width
+constexpr int kSortRadix = 1 << kSortBits;
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 8;                // keys per thread per tile
+constexpr int kSortTile = kSortThreads * kSortItems;
+
+constexpr int kScanThreads = 256;
+constexpr int kScanItems = 8;
+constexpr int kScanTile = kScanThreads * kScanItems;
+
+constexpr int kAsmRows = 32;      // rows per assembly tile
+constexpr int kAsmCap = 768;      // blocks staged per assembly group
+constexpr int kAsmThreads = 256;
+
+constexpr int kSpmvRows = 64;     // rows per SpMV tile
+constexpr int kSpmvCap = 1024;    // blocks staged per SpMV chunk
+constexpr int kSpmvThreads = 256;
+
+constexpr int kVecThreads = 256;
+constexpr int kRedSlots = 4;      // doubles per partial record
+
+// --------------------------------------------------------------- handle ----
+struct Profile {
+  bool on = false;
+  double assemble_ms = 0, spmv_ms = 0, update_ms = 0, solve_ms = 0;
+  int64_t spmv_launches = 0, update_launches = 0, assemble_calls = 0;
+  int64_t solves = 0, iterations = 0;
+};
+
+struct Handle {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  int32_t n = 0;             // vertices
+  int32_t ns = 0;            // springs
+  int32_t max_contacts = 0;
+  int32_t chunk = 16;        // PCG iterations per poll
+  int key_bits = 1;          // bits per vertex index in a sort key
+  int64_t nnzb_static = 0;
+  int64_t nnzb_cap = 0;
+  float gravity[3] = {0, 0, 0};
+  bool assembled = false;
+  float last_dt = 0.f;
+  int sm_count = 0;
+  int spmv_grid = 0, vec_grid = 0;
+  int64_t launches = 0;      // kernels launched by this handle
+  std::string err;
+
+  // static data
+  float* mass = nullptr;         // n
+  int32_t* rowptr_s = nullptr;   // n+1
+  int32_t* colind_s = nullptr;   // nnzb_static
+  int32_t* sblk_ptr = nullptr;   // nnzb_static+1 (range of spring entries)
+  float2* sentry = nullptr;      // 2*ns (k, L0), grouped by static block
+
+  // assembled system
+  int32_t* rowptr = nullptr;     // n+1
+  int32_t* colind = nullptr;     // nnzb_cap (+pad)
+  float* vals = nullptr;         // nnzb_cap*9 (+pad)
+  float* rhs = nullptr;          // 3n
+  float* pinv = nullptr;         // 9n
+
+  // per-step contact workspace (capacity 2*max_contacts entries)
+  uint64_t* ckey[2] = {nullptr, nullptr};
+  int32_t* cval[2] = {nullptr, nullptr};
+  int32_t* sort_counts = nullptr;  // radix * tiles
+  int32_t* flags = nullptr;        // new-block flags, then their prefix
+  int32_t* scan_tmp = nullptr;     // per-tile sums
+  uint64_t* newkey = nullptr;      // keys of new blocks (sorted)
+  int32_t* newfirst = nullptr;     // first sorted entry of each new block
+  int32_t* tile_nb = nullptr;      // per assembly tile: first new block
+  int32_t* tile_eb = nullptr;      // per assembly tile: first contact entry
+  int32_t* counters = nullptr;     // [0] = #new blocks, [1] = #valid entries
+  const uint64_t* skey = nullptr;  // sorted keys of the current step
+  const int32_t* sval = nullptr;   // their contact ids
+  const float* ck = nullptr;       // contact stiffness (caller memory)
+  const float* cr = nullptr;       // contact rest length (caller memory)
+  int32_t nc = 0;
+
+  // host-input staging for pcloth_step_host
+  float* hx = nullptr;
+  float* hv = nullptr;
+  int32_t* hci = nullptr;
+  int32_t* hcj = nullptr;
+  float* hck = nullptr;
+  float* hcr = nullptr;
+
+  // PCG workspace
+  float* dv = nullptr;
+  float* r = nullptr;
+  float* z = nullptr;
+  float* p[2] = {nullptr, nullptr};
+  float* q = nullptr;
+  double* red_spmv = nullptr;      // spmv_grid partials (p.q)
+  double* red_upd[2] = {nullptr, nullptr};  // vec_grid * kRedSlots (r.z, r.r)
+  double* red_init = nullptr;      // vec_grid * kRedSlots (b.b)
+  PcgState* state = nullptr;       // device
+  PcgState* state_host = nullptr;  // pinned, 2 slots
+  uint32_t* d_status = nullptr;    // device error bits
+  uint32_t* h_status = nullptr;    // pinned copy
+
+  // profiling
+  Profile prof;
+  cudaEvent_t ev[8] = {};
+  std::vector<cudaEvent_t> pev;   // per-launch events of two PCG chunks
+  cudaEvent_t chunk_ev[2] = {};
+};
+
+// ------------------------------------------------------------- helpers ----
+int fail(Handle* h, int code, const std::string& msg);
+int cuda_fail(Handle* h, cudaError_t e, const char* what);
+int check_launch(Handle* h, const char* what);
+int collect_status(Handle* h);  // sync + read d_status; returns error code
+
+// radix_sort.cu
+// Stable LSD sort of (key, val) pairs on the low `bits` bits of the keys.
+// Ping-pong between buffers 0 and 1; returns the index holding the result.
+int radix_sort_pairs(Handle* h, uint64_t* keys[2], int32_t* vals[2], int32_t n,
+                     int bits);
+// Exclusive scan of int32 flags in place; writes the total to *total_dev.
+int scan_exclusive(Handle* h, int32_t* data, int32_t n, int32_t* total_dev);
+
+// assemble.cu
+int assemble_system(Handle* h, const float* x, const float* v,
+                    const pcloth_springs* contacts, float dt);
+
+// spmv.cu
+int launch_spmv(Handle* h, const float* in, float* out);
+int launch_spmv_pcg(Handle* h, int k, double tol);  // k = 0-based iteration
+
+// pcg.cu
+int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv,
+              int32_t* iterations, double* rel_residual);
+int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt);
+
+// ---------------------------------------------------------- device code ---
+#ifdef __CUDACC__
+__device__ __forceinline__ bool finite3(float a, float b, float c) {
+  return isfinite(a) && isfinite(b) && isfinite(c);
+}
+
+// Deterministic block-wide sum of one double per thread (fixed tree order).
+template <int THREADS>
+__device__ __forceinline__ double block_sum(double v, double* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  double t = 0.0;
+  if (warp == 0) {
+    t = (lane < THREADS / 32) ? sh[lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+  }
+  __syncthreads();
+  return t;  // valid in thread 0
+}
+
+// Deterministic sum of `count` partial records (slot `slot` of each) that an
+// earlier kernel wrote; every block computes the same value.  Result is
+// broadcast to all threads through shared memory.
+template <int THREADS>
+__device__ __forceinline__ double reduce_partials(const double* part, int count,
+                                                  int stride, int slot,
+                                                  double* sh) {
+  double v = 0.0;
+  for (int t = threadIdx.x; t < count; t += THREADS) v += part[t * stride + slot];
+  v = block_sum<THREADS>(v, sh);
+  if (threadIdx.x == 0) sh[32] = v;
+  __syncthreads();
+  double r = sh[32];
+  __syncthreads();
+  return r;
+}
+#endif
+
+}  // namespace pcloth_impl

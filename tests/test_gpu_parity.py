@@ -1,0 +1,252 @@
+"""GPU path (through the C ABI) against the fp64 oracle on identical seeded
+inputs.  P-Cloth (arXiv 2008.00409): Sec. 2.5 Eq. (3) (system), Sec. 3.2.2
+(pattern and value filling), Sec. 3.1 (SpMV and PCG).
+
+Tolerances (fp32 storage and arithmetic against fp64):
+  * pattern (rowptr, colind): bit-exact;
+  * assembled blocks: max per-block relative Frobenius error <= 1e-5;
+  * b: <= 1e-5 relative to the summed magnitude of its terms per vertex;
+  * block-Jacobi inverses: per block within the perturbation bound
+    kappa(D) (|dD|/|D| + 16 eps32) of a matrix inverse, and P D = I to
+    16 kappa(D) eps32 against the GPU's own diagonal block;
+  * SpMV: relative L2 <= 1e-5;
+  * PCG: same algorithm and tolerance on both sides, relative L2 of dv
+    <= 1e-4 and iteration counts within max(3, 3%).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from sparse_linear_solve_gb300 import pcloth as pc
+from sparse_linear_solve_gb300 import workloads as W
+
+from gpu_helpers import DEV, compare_assembly, make, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def small_configs():
+    return {
+        "tiny32": W.tiny_cloth(),
+        "tiny32_tension": W.tiny_cloth(rest_from_grid=True),
+        "droop37": W.drooped_cloth(n=37, steps=2),          # ragged tiles
+        "jitter64": W.jittered_cloth(n=64, steps=2),
+        "twolayer33": W.two_layer_cloth(n=33, steps=2),
+        "folded4x29": W.folded_stack(n=29, steps=2),
+    }
+
+
+@pytest.mark.parametrize("name", list(small_configs()))
+def test_assembly_matches_oracle(name):
+    w = small_configs()[name]
+    c = w.contacts(0)
+    compare_assembly(w, w.x0, w.v0, c if c.n else None)
+
+
+@pytest.mark.parametrize("name", list(small_configs()))
+def test_spmv_matches_oracle(name):
+    w = small_configs()[name]
+    c = w.contacts(0)
+    pcl, ref, _, _ = compare_assembly(w, w.x0, w.v0, c if c.n else None)
+    rng = np.random.default_rng(11)
+    for _ in range(2):
+        x = rng.normal(size=(w.n_verts, 3)).astype(np.float32)
+        y = pcl.spmv(to_dev(x)).cpu().numpy()
+        e = rel_l2(y, ref.spmv(x))
+        assert e <= 1e-5, e
+
+
+@pytest.mark.parametrize("name", list(small_configs()))
+def test_pcg_matches_oracle(name):
+    w = small_configs()[name]
+    c = w.contacts(0)
+    pcl, ref, _, _ = compare_assembly(w, w.x0, w.v0, c if c.n else None)
+    dv_ref, it_ref, rr_ref, st_ref = ref.pcg(w.tol, w.maxit)
+    assert st_ref == oracle.OK
+    dv, it, rr, code = pcl.solve(w.tol, w.maxit)
+    assert code == pc.OK and rr <= w.tol
+    e = rel_l2(dv.cpu().numpy(), dv_ref)
+    assert e <= 1e-4, (e, it, it_ref)
+    assert abs(it - it_ref) <= max(3, 0.03 * it_ref), (it, it_ref)
+
+
+def test_multistep_per_step_parity():
+    """Per-step parity on identical inputs over several steps with changing
+    contacts: each step both sides start from the oracle's state."""
+    w = W.jittered_cloth(n=48, steps=3)
+    pcl = make(w)
+    x, v = w.x0, w.v0
+    for step in range(3):
+        c = w.contacts(step)
+        res = oracle.step(w, x, v, c)
+        assert res["status"] == oracle.OK
+        xd, vd = to_dev(x), to_dev(v)
+        dv = torch.empty_like(xd)
+        it, rr, code = pcl.step(xd, vd, c, w.h, w.tol, w.maxit, dv)
+        assert code == pc.OK
+        assert rel_l2(dv.cpu().numpy(), res["dv"]) <= 1e-4
+        assert rel_l2(vd.cpu().numpy(), res["v"]) <= 1e-4
+        assert rel_l2(xd.cpu().numpy(), res["x"]) <= 1e-6
+        x, v = res["x"].astype(np.float32), res["v"].astype(np.float32)
+
+
+def test_contacts_duplicates_and_spring_pairs():
+    """Contacts repeated, reversed and on existing spring pairs merge into
+    one block each (filling step 3) with summed values."""
+    w = W.tiny_cloth(n=16, rest_from_grid=True)
+    a, b = int(w.spring_i[5]), int(w.spring_j[5])
+    ci = np.array([a, 3, 40, 3, b, 7], np.int32)
+    cj = np.array([b, 40, 3, 40, a, 200], np.int32)
+    ck = np.array([1e3, 1e3, 5e2, 2e2, 1e3, 1e3], np.float32)
+    cr = np.array([2e-3, 3e-3, 4e-3, 5e-3, 1e-3, 2e-3], np.float32)
+    c = W.Contacts(ci, cj, ck, cr)
+    w.max_contacts = 16
+    compare_assembly(w, w.x0, w.v0, c)
+
+
+def test_long_rows_exercise_chunked_paths():
+    """One vertex in contact with 1500 others: its row is longer than the
+    assembly staging and the SpMV chunk, and a tile exceeds both."""
+    w = W.tiny_cloth(n=48, rest_from_grid=True)
+    N = w.n_verts
+    hub = N // 2 + 7
+    others = np.array([j for j in range(N) if j != hub][:1500], np.int32)
+    rng = np.random.default_rng(5)
+    c = W.Contacts(np.full(len(others), hub, np.int32), others,
+                   rng.uniform(1e2, 1e3, len(others)).astype(np.float32),
+                   rng.uniform(1e-3, 5e-2, len(others)).astype(np.float32))
+    w.max_contacts = len(others)
+    pcl, ref, g, _ = compare_assembly(w, w.x0, w.v0, c)
+    assert int(g["rowptr"][hub + 1] - g["rowptr"][hub]) > 1024
+    x = np.random.default_rng(2).normal(size=(N, 3)).astype(np.float32)
+    assert rel_l2(pcl.spmv(to_dev(x)).cpu().numpy(), ref.spmv(x)) <= 1e-5
+    dv_ref, it_ref, _, _ = ref.pcg(w.tol, w.maxit)
+    dv, it, rr, code = pcl.solve(w.tol, w.maxit)
+    assert code == pc.OK
+    assert rel_l2(dv.cpu().numpy(), dv_ref) <= 1e-4
+
+
+def test_pattern_rebuilt_in_place_across_steps():
+    """The pattern grows and shrinks with the contacts, always matching the
+    oracle, inside the buffers allocated at create."""
+    w = W.jittered_cloth(n=40)
+    pcl = make(w)
+    for step in range(4):
+        c = w.contacts(step) if step != 2 else None
+        compare_assembly(w, w.x0, w.v0, c, pcl=pcl)
+    # back to no contacts: the static pattern
+    _, ref, _, _ = compare_assembly(w, w.x0, w.v0, None, pcl=pcl)
+    assert ref.nnzb == w.n_verts + 2 * w.n_springs
+
+
+def test_deterministic_bitwise():
+    w = W.folded_stack(n=24)
+    c = w.contacts(1)
+    outs = []
+    for _ in range(2):
+        pcl = make(w)
+        xd, vd = to_dev(w.x0), to_dev(w.v0)
+        pcl.assemble(xd, vd, c, w.h)
+        g = pcl.export()
+        dv, it, rr, _ = pcl.solve(w.tol, w.maxit)
+        outs.append((g["vals"].cpu().numpy(), g["b"].cpu().numpy(), dv.cpu().numpy(), it, rr))
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(np.asarray(a), np.asarray(b))
+
+
+def test_zero_stiffness_one_iteration():
+    w = W.tiny_cloth(n=12)
+    w.spring_k[:] = 0.0
+    pcl = make(w)
+    xd, vd = to_dev(w.x0), to_dev(w.v0)
+    pcl.assemble(xd, vd, None, w.h)
+    dv, it, rr, code = pcl.solve(1e-6, 100)
+    assert code == pc.OK and it == 1
+    np.testing.assert_allclose(dv.cpu().numpy(), np.tile(w.h * w.gravity, (w.n_verts, 1)),
+                               rtol=1e-6)
+
+
+def test_zero_rhs_returns_zero_iterations():
+    w = W.tiny_cloth(n=10, rest_from_grid=False)
+    w.gravity[:] = 0.0
+    pcl = make(w)
+    xd = to_dev(w.x0)
+    vd = torch.zeros_like(xd)
+    pcl.assemble(xd, vd, None, w.h)
+    dv, it, rr, code = pcl.solve(1e-6, 100)
+    # springs at rest, no velocity, no gravity: b is (numerically) zero or tiny
+    assert code == pc.OK
+    if it == 0:
+        assert float(dv.abs().max()) == 0.0
+
+
+def test_maxit_and_error_codes():
+    w = W.tiny_cloth(n=20, rest_from_grid=True)
+    w.max_contacts = 2
+    pcl = make(w)
+    xd, vd = to_dev(w.x0), to_dev(w.v0)
+    pcl.assemble(xd, vd, None, w.h)
+    dv, it, rr, code = pcl.solve(1e-12, 1)
+    assert code == pc.NOT_CONVERGED and it == 1 and rr > 1e-12
+    dv, it, rr, code = pcl.solve(1e-6, 0)
+    assert code == pc.NOT_CONVERGED and it == 0 and abs(rr - 1.0) < 1e-12
+    # out-of-range, self contact
+    for ci, cj in ((0, w.n_verts), (-1, 3), (4, 4)):
+        bad = W.Contacts(np.array([ci], np.int32), np.array([cj], np.int32),
+                         np.array([1.0], np.float32), np.array([0.1], np.float32))
+        pcl.assemble(xd, vd, bad, w.h)
+        with pytest.raises(pc.PClothError) as ei:
+            pcl.nnzb()
+        assert ei.value.code == pc.ERR_BAD_INDEX
+    # more contacts than max_contacts
+    many = W.Contacts(np.zeros(3, np.int32), np.ones(3, np.int32),
+                      np.ones(3, np.float32), np.ones(3, np.float32))
+    with pytest.raises(pc.PClothError) as ei:
+        pcl.assemble(xd, vd, many, w.h)
+    assert ei.value.code == pc.ERR_CAPACITY
+    # NaN velocity
+    vbad = vd.clone()
+    vbad[3, 1] = float("nan")
+    pcl.assemble(xd, vbad, None, w.h)
+    with pytest.raises(pc.PClothError) as ei:
+        pcl.solve(1e-6, 100)
+    assert ei.value.code == pc.ERR_NONFINITE
+    # the handle is usable again afterwards
+    pcl.assemble(xd, vd, None, w.h)
+    dv, it, rr, code = pcl.solve(1e-6, 10000)
+    assert code == pc.OK
+
+
+def test_solve_before_assemble_is_rejected():
+    w = W.tiny_cloth(n=8)
+    pcl = make(w)
+    with pytest.raises(pc.PClothError) as ei:
+        pcl.solve(1e-6, 10)
+    assert ei.value.code == pc.ERR_STATE
+
+
+def test_step_host_matches_device_step():
+    w = W.jittered_cloth(n=40)
+    c = w.contacts(0)
+    pcl = make(w)
+    xd, vd = to_dev(w.x0), to_dev(w.v0)
+    it_d, rr_d, _ = pcl.step(xd, vd, c, w.h, w.tol, w.maxit)
+    xh = torch.from_numpy(w.x0.copy()).pin_memory()
+    vh = torch.from_numpy(w.v0.copy()).pin_memory()
+    it_h, rr_h, _ = pcl.step_host(xh, vh, c, w.h, w.tol, w.maxit)
+    assert it_h == it_d and rr_h == rr_d
+    assert torch.equal(xh, xd.cpu()) and torch.equal(vh, vd.cpu())
+
+
+def test_chunk_size_does_not_change_results():
+    w = W.drooped_cloth(n=30)
+    res = []
+    for chunk in (1, 7, 64):
+        pcl = make(w, chunk=chunk)
+        xd, vd = to_dev(w.x0), to_dev(w.v0)
+        pcl.assemble(xd, vd, None, w.h)
+        dv, it, rr, _ = pcl.solve(w.tol, w.maxit)
+        res.append((dv.cpu().numpy(), it, rr))
+    for r in res[1:]:
+        assert np.array_equal(r[0], res[0][0]) and r[1] == res[0][1] and r[2] == res[0][2]
