@@ -222,12 +222,12 @@ def run_ours(args, rank, world, local_rank):
     n = w.n_verts
     nnzb = nnzb_seen[-1]
     bytes_per_launch = 40 * nnzb + 52 * n
-    launches = max(prof["spmv_launches"], 1)
-    spmv_avg_ms = prof["spmv_ms"] / launches
+    samples = max(prof["samples"], 1)
+    spmv_avg_ms = prof["spmv_ms"] / samples
     achieved = bytes_per_launch / (spmv_avg_ms * 1e-3) / 1e9
     peak, peak_src = hbm_peak()
     upd_bytes = 120 * n  # dv, p, r, q, P(36) read; dv, r, z written (bytes/vertex)
-    upd_avg_ms = prof["update_ms"] / max(prof["update_launches"], 1)
+    upd_avg_ms = prof["update_ms"] / samples
 
     # ---- end to end through the host-buffer entry point ------------------
     e2e = None
@@ -241,12 +241,17 @@ def run_ours(args, rank, world, local_rank):
                                 for a in (c.i, c.j, c.k, c.rest)))
             else:
                 hc.append(None)
-        cloth.step_host(xh, vh, hc[0], w.h, w.tol, w.maxit)  # warm
+        # the same trajectory as the device-timed leg: same warm-up steps from
+        # the same initial state, then the same K steps, so the iteration
+        # counts (and so the work) are identical
+        e2e_its = []
+        for t in range(Wm):
+            cloth.step_host(xh, vh, hc[t], w.h, w.tol, w.maxit)
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
         for t in range(K):
-            cloth.step_host(xh, vh, hc[Wm + t], w.h, w.tol, w.maxit)
+            e2e_its.append(cloth.step_host(xh, vh, hc[Wm + t], w.h, w.tol, w.maxit)[0])
         t1 = time.perf_counter()
         e_s = t1 - t0
         if world > 1:
@@ -256,7 +261,8 @@ def run_ours(args, rank, world, local_rank):
         nc_mean = sum(c.n for c in host_contacts[Wm:]) / K
         e2e = dict(value=world * K / e_s, unit=UNIT,
                    h2d_bytes_per_step=int(2 * 12 * n + 16 * nc_mean),
-                   d2h_bytes_per_step=int(2 * 12 * n))
+                   d2h_bytes_per_step=int(2 * 12 * n),
+                   pcg_iterations_mean=sum(e2e_its) / K)
 
     result = dict(
         metric=METRIC, value=world * K / (ms * 1e-3), unit=UNIT, n_gpus=world, steps=K,
@@ -275,7 +281,10 @@ def run_ours(args, rank, world, local_rank):
         update_us=upd_avg_ms * 1e3,
         update_gbs=upd_bytes / (upd_avg_ms * 1e-3) / 1e9 if upd_avg_ms > 0 else None,
         codes=sorted(set(codes)),
-        roofline=dict(bound="hbm", kernel="spmv_tiles<true> (PCG SpMV, fused p update + p.q)",
+        roofline=dict(bound="hbm", kernel="spmv_pipe<true> (PCG SpMV, fused p update + p.q)",
+                      timing="CUDA events on the library stream around the SpMV of the first "
+                             "PCG iteration of every %d-iteration chunk (%d samples)"
+                             % (16, prof["samples"]),
                       achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
                       peak_source=peak_src, bytes_per_launch=bytes_per_launch,
                       bytes_model="40 B/block (36 values + 4 colind) + 52 B/row (rowptr 4, "

@@ -165,11 +165,14 @@ int pcloth_sync(pcloth_t h);
 const char* pcloth_last_error(pcloth_t h);
 
 /* Profiling: while enabled, the library records CUDA events on its stream
- * around every assembly, SpMV and PCG-update launch and accumulates their
- * device time.  pcloth_profile_read fills ms_out[4] = {assembly, PCG SpMV,
- * PCG update, whole solves} in milliseconds and counts_out[6] =
- * {assemblies, SpMV launches, update launches, solves, PCG iterations,
- * kernels launched by this handle}; reset != 0 zeroes the accumulators. */
+ * around every assembly and solve, and around the two launches (SpMV, PCG
+ * update) of the first iteration of every polling chunk, and accumulates
+ * their device time.  pcloth_profile_read fills ms_out[4] = {assembly,
+ * sampled PCG SpMV, sampled PCG update, whole solves} in milliseconds and
+ * counts_out[7] = {assemblies, SpMV launches, update launches, solves, PCG
+ * iterations, kernels launched by this handle, sampled iterations}; divide
+ * the sampled times by the sample count for a per-launch average.
+ * reset != 0 zeroes the accumulators. */
 int pcloth_profile_enable(pcloth_t h, int on);
 int pcloth_profile_read(pcloth_t h, double* ms_out, int64_t* counts_out,
                         int reset);

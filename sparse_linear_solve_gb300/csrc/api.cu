@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -32,12 +33,12 @@ void free_handle(Handle* h) {
   cudaSetDevice(h->device);
   cudaStreamSynchronize(h->stream);
   void* bufs[] = {h->mass, h->rowptr_s, h->colind_s, h->sblk_ptr, h->sentry,
-                  h->rowptr, h->colind, h->vals, h->rhs, h->pinv,
+                  h->rowptr, h->colind, h->vals, h->rhs, h->pinv8,
                   h->ckey[0], h->ckey[1], h->cval[0], h->cval[1],
                   h->sort_counts, h->flags, h->scan_tmp, h->newkey,
                   h->newfirst, h->tile_nb, h->tile_eb, h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
-                  h->dv, h->r, h->z, h->p[0], h->p[1], h->q, h->red_spmv,
+                  h->dv, h->dv4, h->r4, h->z4, h->p4[0], h->p4[1], h->q4, h->red_spmv,
                   h->red_upd[0], h->red_upd[1], h->red_init, h->state,
                   h->d_status};
   for (void* b : bufs)
@@ -207,8 +208,10 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   const int64_t sort_tiles = (ent2 + kSortTile - 1) / kSortTile;
   const int64_t scan_tiles = (ent2 + kScanTile - 1) / kScanTile;
   const int64_t asm_tiles = (n + kAsmRows - 1) / kAsmRows;
-  h->spmv_grid = int(std::min<int64_t>((n + kSpmvRows - 1) / kSpmvRows, int64_t(h->sm_count) * 4));
-  h->vec_grid = int(std::min<int64_t>((3 * n + kVecThreads - 1) / kVecThreads, int64_t(h->sm_count) * 4));
+  h->spmv_grid = spmv_grid_for(int32_t(n), h->sm_count);
+  const int64_t red_grid = h->spmv_grid;
+  h->vec_grid = int(std::min<int64_t>((n + kVecThreads - 1) / kVecThreads,
+                                      int64_t(h->sm_count) * 4));
   const int64_t vpad = 64;  // floats of slack after each vector / value array
   bool ok = true;
   auto A = [&](cudaError_t r) { ok = ok && (r == cudaSuccess); };
@@ -221,11 +224,11 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->colind, cap + vpad));
   A(dalloc(&h->vals, cap * 9 + vpad));
   A(dalloc(&h->rhs, 3 * n + vpad));
-  A(dalloc(&h->pinv, 9 * n + vpad));
+  A(dalloc(&h->pinv8, 2 * n + vpad));
   for (int b = 0; b < 2; ++b) {
     A(dalloc(&h->ckey[b], ent2));
     A(dalloc(&h->cval[b], ent2));
-    A(dalloc(&h->p[b], 3 * n + vpad));
+    A(dalloc(&h->p4[b], n + vpad));
     A(dalloc(&h->red_upd[b], int64_t(h->vec_grid) * kRedSlots));
   }
   A(dalloc(&h->sort_counts, sort_tiles * kSortRadix + 1));
@@ -243,10 +246,11 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->hck, std::max<int64_t>(mc, 1)));
   A(dalloc(&h->hcr, std::max<int64_t>(mc, 1)));
   A(dalloc(&h->dv, 3 * n + vpad));
-  A(dalloc(&h->r, 3 * n + vpad));
-  A(dalloc(&h->z, 3 * n + vpad));
-  A(dalloc(&h->q, 3 * n + vpad));
-  A(dalloc(&h->red_spmv, int64_t(h->spmv_grid) * kRedSlots));
+  A(dalloc(&h->dv4, n + vpad));
+  A(dalloc(&h->r4, n + vpad));
+  A(dalloc(&h->z4, n + vpad));
+  A(dalloc(&h->q4, n + vpad));
+  A(dalloc(&h->red_spmv, red_grid * kRedSlots));
   A(dalloc(&h->red_init, int64_t(h->vec_grid) * kRedSlots));
   A(dalloc(&h->state, 1));
   A(dalloc(&h->d_status, 1));
@@ -273,9 +277,11 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   if (e == cudaSuccess) e = cudaMemset(h->vals, 0, (cap * 9 + vpad) * 4);
   if (e == cudaSuccess) e = cudaMemset(h->colind, 0, (cap + vpad) * 4);
   if (e == cudaSuccess) e = cudaMemset(h->rowptr, 0, (n + 1 + vpad) * 4);
-  for (float* v : {h->dv, h->r, h->z, h->q, h->p[0], h->p[1], h->rhs})
+  for (float* v : {h->dv, h->rhs})
     if (e == cudaSuccess) e = cudaMemset(v, 0, (3 * n + vpad) * 4);
-  if (e == cudaSuccess) e = cudaMemset(h->pinv, 0, (9 * n + vpad) * 4);
+  for (float4* v : {h->dv4, h->r4, h->z4, h->q4, h->p4[0], h->p4[1]})
+    if (e == cudaSuccess) e = cudaMemset(v, 0, (n + vpad) * sizeof(float4));
+  if (e == cudaSuccess) e = cudaMemset(h->pinv8, 0, (2 * n + vpad) * sizeof(float4));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->state, 0, sizeof(PcgState));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -410,9 +416,12 @@ int pcloth_export(pcloth_t ht, int32_t* rowptr, int32_t* colind, float* vals,
     e = cudaMemcpyAsync(vals, h->vals, size_t(nnzb) * 36, cudaMemcpyDefault, h->stream);
   if (b && e == cudaSuccess)
     e = cudaMemcpyAsync(b, h->rhs, n * 12, cudaMemcpyDefault, h->stream);
-  if (pinv && e == cudaSuccess)
-    e = cudaMemcpyAsync(pinv, h->pinv, n * 36, cudaMemcpyDefault, h->stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "export copy");
+  if (pinv) {
+    rc = launch_pinv_expand(h, pinv);
+    if (rc != PCLOTH_OK) return rc;
+  }
+  e = cudaStreamSynchronize(h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "export copy");
   return PCLOTH_OK;
 }
@@ -464,6 +473,7 @@ int pcloth_profile_read(pcloth_t ht, double* ms_out, int64_t* counts_out, int re
     counts_out[3] = h->prof.solves;
     counts_out[4] = h->prof.iterations;
     counts_out[5] = h->launches;
+    counts_out[6] = h->prof.samples;
   }
   if (reset) {
     bool on = h->prof.on;

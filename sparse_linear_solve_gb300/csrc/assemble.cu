@@ -56,7 +56,7 @@ struct AsmArgs {
   int32_t* colind;
   float* vals;
   float* rhs;
-  float* pinv;
+  float4* pinv8;
   uint32_t* status;
 };
 
@@ -146,43 +146,87 @@ __global__ void tile_bounds(int32_t ntiles, int32_t n, int B, int has_contacts,
   tile_eb[t] = lower_bound_key(skey, 0, counters[1], key);
 }
 
-// Length minus rest length, l - L0 = (|e|^2 - L0^2) / (l + L0), with the
-// squares summed in fp64 (exact for fp32 components).  Near the rest length
-// the plain fp32 difference l - L0 is pure rounding noise (~1e-7 L0); that
-// noise would give a spring at rest a spurious transverse stiffness
-// k (1 - L0/l) (I - d d^T) along exactly the soft out-of-plane directions of
-// a flat sheet, whose only other stiffness is the mass term.
-__device__ __forceinline__ float stretch_of(float3 e, float l, float L0) {
-  const double d2 = double(e.x) * e.x + double(e.y) * e.y + double(e.z) * e.z -
-                    double(L0) * L0;
-  return float(d2) / (l + L0);
+// An edge vector carried exactly as hi + lo: the difference of two fp32
+// coordinates is rounded in fp32, and near the rest shape of a flat sheet
+// that rounding alone (a tilt of the spring axis by ~1e-8) shifts the
+// solution along the soft out-of-plane modes by ~1e-4.  TwoSum recovers the
+// rounding error exactly; x_i - x_j gives exactly (-hi, -lo), so the blocks
+// (i, j) and (j, i) stay bitwise equal.
+struct Edge {
+  float3 hi, lo;
+};
+
+__device__ __forceinline__ float two_diff_lo(float a, float b, float s) {  // s = fl(a - b)
+  const float bp = s - a;
+  return (a - (s - bp)) + (-b - bp);
 }
 
-// K (6 unique entries of the symmetric 3x3 block) and F of one element seen
-// from vertex i: K at x, force at x~ = x + h v.  e = x_j - x_i is passed in
-// (it is shared by all elements of a block) and w = v_j - v_i.  The advanced
-// edge is formed as e + h w, not as a difference of advanced positions, so
-// it keeps the accuracy of the short edge instead of that of the (possibly
-// metres-large) coordinates; both l - L0 and l~ - L0 come from stretch_of.
-__device__ __forceinline__ void element_terms(float3 e, float3 w, float dt, float k, float L0,
-                                              float (&K)[6], float (&F)[3]) {
-  const float l = sqrtf(e.x * e.x + e.y * e.y + e.z * e.z);
-  const float inv = 1.0f / l;
-  const float dx = e.x * inv, dy = e.y * inv, dz = e.z * inv;
-  const float tension = fmaxf(0.0f, stretch_of(e, l, L0) * inv);   // max(0, 1 - L0/l)
-  const float a = k * tension;        // k * max(0, 1 - L0/l)
-  const float c = k - a;              // k * (1 - max(...))
-  K[0] += a + c * dx * dx;
-  K[1] += c * dx * dy;
-  K[2] += c * dx * dz;
-  K[3] += a + c * dy * dy;
-  K[4] += c * dy * dz;
-  K[5] += a + c * dz * dz;
-  const float3 f = make_float3(fmaf(dt, w.x, e.x), fmaf(dt, w.y, e.y), fmaf(dt, w.z, e.z));
-  const float fx = f.x, fy = f.y, fz = f.z;
+__device__ __forceinline__ Edge edge_of(float3 xi, float3 xj) {
+  Edge e;
+  e.hi = make_float3(xj.x - xi.x, xj.y - xi.y, xj.z - xi.z);
+  e.lo = make_float3(two_diff_lo(xj.x, xi.x, e.hi.x), two_diff_lo(xj.y, xi.y, e.hi.y),
+                     two_diff_lo(xj.z, xi.z, e.hi.z));
+  return e;
+}
+
+// |e|^2 - L0^2 in fp64 from an exact edge (hi + lo is exact in fp64 and its
+// square is accurate to fp64 rounding).
+__device__ __forceinline__ double excess_sq(float3 hi, float3 lo, float L0) {
+  const double x = double(hi.x) + lo.x, y = double(hi.y) + lo.y, z = double(hi.z) + lo.z;
+  return x * x + y * y + z * z - double(L0) * L0;
+}
+
+// Scaled stiffness block K' = -h^2 K (6 unique entries of the symmetric
+// block) and force F of one element seen from vertex i: K at x, force at
+// x~ = x + h v.  e = x_j - x_i (exact, see Edge) is shared by all elements of
+// a block and w = v_j - v_i.
+//
+// K = a I + c d d^T with a = k max(0, 1 - L0/l), c = k - a.  The length
+// excess l - L0 is formed as (|e|^2 - L0^2) / (l + L0) with the squares in
+// fp64: near the rest length the plain fp32 difference is pure rounding noise
+// (~1e-7 L0) that would give a spring at rest a spurious transverse stiffness
+// along exactly the soft out-of-plane directions of a flat sheet.  Written
+// as K' = A I + S e e^T with A = -h^2 a and S = -h^2 c / l^2, each product
+// e_r e_c is formed in double-float (exact hi*hi by an FMA plus the hi*lo
+// cross terms) and scaled by S with about one rounding; any error in S is
+// common to the whole e e^T term, so the block keeps its rank-one-plus-
+// identity structure.
+//
+// The advanced edge is formed as e + h w, not as a difference of advanced
+// positions, so it keeps the accuracy of the short edge instead of that of
+// the (possibly metres-large) coordinates.
+__device__ __forceinline__ float scaled_entry(float S, float hr, float lr, float hc, float lc) {
+  const float p = hr * hc;
+  const float pe = fmaf(hr, hc, -p);             // hr * hc == p + pe exactly
+  const float tail = pe + fmaf(hr, lc, lr * hc);
+  return fmaf(S, p, S * tail);
+}
+
+__device__ __forceinline__ void element_terms(const Edge& e, float3 w, float dt, float h2,
+                                              float k, float L0, float (&K)[6], float (&F)[3]) {
+  const float3 h = e.hi, o = e.lo;
+  const float l2 = fmaf(h.x, h.x, fmaf(h.y, h.y, h.z * h.z)) +
+                   2.0f * fmaf(h.x, o.x, fmaf(h.y, o.y, h.z * o.z));
+  const float l = sqrtf(l2);
+  const float stretch = float(excess_sq(h, o, L0)) / (l + L0);    // l - L0
+  const float tension = fmaxf(0.0f, stretch / l);                  // max(0, 1 - L0/l)
+  const float a = k * tension;
+  const float c = k - a;
+  const float A = -h2 * a;
+  const float S = (-h2 * c) / l2;
+  K[0] += scaled_entry(S, h.x, o.x, h.x, o.x) + A;
+  K[1] += scaled_entry(S, h.x, o.x, h.y, o.y);
+  K[2] += scaled_entry(S, h.x, o.x, h.z, o.z);
+  K[3] += scaled_entry(S, h.y, o.y, h.y, o.y) + A;
+  K[4] += scaled_entry(S, h.y, o.y, h.z, o.z);
+  K[5] += scaled_entry(S, h.z, o.z, h.z, o.z) + A;
+  // force at the advanced positions
+  const float fx = fmaf(dt, w.x, h.x) + o.x, fy = fmaf(dt, w.y, h.y) + o.y,
+              fz = fmaf(dt, w.z, h.z) + o.z;
   const float lt = sqrtf(fx * fx + fy * fy + fz * fz);
-  const float stretch = stretch_of(f, lt, L0);   // l~ - L0
-  const float s = k * stretch / lt;
+  const float3 fz3 = make_float3(0.f, 0.f, 0.f);
+  const float st = float(excess_sq(make_float3(fx, fy, fz), fz3, L0)) / (lt + L0);   // l~ - L0
+  const float s = k * st / lt;
   F[0] += s * fx;
   F[1] += s * fy;
   F[2] += s * fz;
@@ -213,7 +257,7 @@ struct RowInfo {
 };
 
 // Computes block `o` (absolute output index) of tile-local row `ri`; writes
-// the value (9 floats, -h^2 K sum) and the force sum into shared staging.
+// the value (9 floats, -h^2 sum K) and the force sum into shared staging.
 __device__ __forceinline__ void compute_block(const AsmArgs& a, int32_t i, const RowInfo& R,
                                               int32_t p, float* __restrict__ stv,
                                               float* __restrict__ stf, int32_t* __restrict__ stc,
@@ -239,13 +283,13 @@ __device__ __forceinline__ void compute_block(const AsmArgs& a, int32_t i, const
   if (col != i) {
     const float3 xi = ld3(a.x, i), vi = ld3(a.v, i);
     const float3 xj = ld3(a.x, col), vj = ld3(a.v, col);
-    const float3 ed = make_float3(xj.x - xi.x, xj.y - xi.y, xj.z - xi.z);
+    const Edge ed = edge_of(xi, xj);
     const float3 wd = make_float3(vj.x - vi.x, vj.y - vi.y, vj.z - vi.z);
     if (sslot >= 0) {
       const int32_t e1 = a.sblk_ptr[sslot + 1];
       for (int32_t e = a.sblk_ptr[sslot]; e < e1; ++e) {
         const float2 kl = a.sentry[e];
-        element_terms(ed, wd, a.dt, kl.x, kl.y, K, F);
+        element_terms(ed, wd, a.dt, a.h2, kl.x, kl.y, K, F);
       }
     }
     // contacts on this (row, col) pair: a run of equal sorted keys
@@ -260,26 +304,31 @@ __device__ __forceinline__ void compute_block(const AsmArgs& a, int32_t i, const
     if (t0 >= 0) {
       for (int32_t t = t0; t < m_valid && a.skey[t] == key; ++t) {
         const int32_t c = a.sval[t];
-        element_terms(ed, wd, a.dt, a.ck[c], a.cr[c], K, F);
+        element_terms(ed, wd, a.dt, a.h2, a.ck[c], a.cr[c], K, F);
       }
     }
   }
-  const float h2 = a.h2;
-  stv[0] = -h2 * K[0]; stv[1] = -h2 * K[1]; stv[2] = -h2 * K[2];
-  stv[3] = -h2 * K[1]; stv[4] = -h2 * K[3]; stv[5] = -h2 * K[4];
-  stv[6] = -h2 * K[2]; stv[7] = -h2 * K[4]; stv[8] = -h2 * K[5];
+  stv[0] = K[0]; stv[1] = K[1]; stv[2] = K[2];
+  stv[3] = K[1]; stv[4] = K[3]; stv[5] = K[4];
+  stv[6] = K[2]; stv[7] = K[4]; stv[8] = K[5];
   stf[0] = F[0]; stf[1] = F[1]; stf[2] = F[2];
   *stc = col;
 }
 
 // Diagonal block, right-hand side and block-Jacobi inverse of row i from the
-// accumulated off-diagonal sums (Ks = h^2 sum K, 6 unique entries) and force.
+// row's compensated sum h^2 sum K = Ks + Kc (6 unique entries, Kc the
+// TwoSum compensation) and its force sum.  The mass is added to the small
+// compensation term first, so the diagonal is rounded once from the exact
+// total: adding m after rounding the large sum would round the same m to the
+// same ulp grid in every row of a binade -- a coherent shift of the mass by
+// ~0.1%, which the soft modes of the system amplify.
 __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const float (&Ks)[6],
-                                           const float (&Fs)[3], float* __restrict__ D) {
+                                           const float (&Kc)[6], const float (&Fs)[3],
+                                           float* __restrict__ D) {
   const float m = a.mass[i];
-  D[0] = m + Ks[0]; D[1] = Ks[1]; D[2] = Ks[2];
-  D[3] = Ks[1]; D[4] = m + Ks[3]; D[5] = Ks[4];
-  D[6] = Ks[2]; D[7] = Ks[4]; D[8] = m + Ks[5];
+  D[0] = Ks[0] + (Kc[0] + m); D[1] = Ks[1] + Kc[1]; D[2] = Ks[2] + Kc[2];
+  D[3] = D[1]; D[4] = Ks[3] + (Kc[3] + m); D[5] = Ks[4] + Kc[4];
+  D[6] = D[2]; D[7] = D[5]; D[8] = Ks[5] + (Kc[5] + m);
   const float b0 = a.dt * (Fs[0] + m * a.gx);
   const float b1 = a.dt * (Fs[1] + m * a.gy);
   const float b2 = a.dt * (Fs[2] + m * a.gz);
@@ -295,10 +344,9 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const fl
   const float c22 = D[0] * D[4] - D[1] * D[3];
   const float det = D[0] * c00 + D[1] * c01 + D[2] * c02;
   const float id = 1.0f / det;
-  float* P = a.pinv + 9 * int64_t(i);
-  P[0] = c00 * id; P[1] = c01 * id; P[2] = c02 * id;
-  P[3] = c01 * id; P[4] = c11 * id; P[5] = c12 * id;
-  P[6] = c02 * id; P[7] = c12 * id; P[8] = c22 * id;
+  // the inverse of a symmetric block is symmetric: six entries, two float4
+  a.pinv8[2 * int64_t(i)] = make_float4(c00 * id, c01 * id, c02 * id, c11 * id);
+  a.pinv8[2 * int64_t(i) + 1] = make_float4(c12 * id, c22 * id, 0.f, 0.f);
   bool ok = finite3(b0, b1, b2) && isfinite(det) && det > 0.0f;
 #pragma unroll
   for (int t = 0; t < 9; ++t) ok = ok && isfinite(D[t]);
@@ -311,8 +359,8 @@ assemble_rows(AsmArgs a) {
   __shared__ float stv[kAsmCap * 9];
   __shared__ float stf[kAsmCap * 3];
   __shared__ int32_t stc[kAsmCap];
-  __shared__ float red[9][kAsmThreads / 32];
-  __shared__ float acc[9];
+  __shared__ double red[9][kAsmThreads / 32];
+  __shared__ double acc[9];
 
   const int32_t r0 = blockIdx.x * kAsmRows;
   const int32_t nrows = min(kAsmRows, a.n - r0);
@@ -371,17 +419,26 @@ assemble_rows(AsmArgs a) {
       for (int32_t ri = g + threadIdx.x; ri < e; ri += kAsmThreads) {
         const int32_t i = r0 + ri;
         const int32_t o0 = rows[ri].ob - gob, o1 = rows[ri + 1].ob - gob;
-        float Ks[6] = {0, 0, 0, 0, 0, 0}, Fs[3] = {0, 0, 0};
+        // h^2 sum K over the row, compensated (TwoSum): the diagonal is
+        // ~h^2 k while the mass it must preserve is far smaller
+        float Ks[6] = {0, 0, 0, 0, 0, 0}, Kc[6] = {0, 0, 0, 0, 0, 0}, Fs[3] = {0, 0, 0};
         int32_t dpos = -1;
         for (int32_t o = o0; o < o1; ++o) {
           if (stc[o] == i) { dpos = o; continue; }
           const float* s = &stv[9 * o];
-          Ks[0] -= s[0]; Ks[1] -= s[1]; Ks[2] -= s[2];
-          Ks[3] -= s[4]; Ks[4] -= s[5]; Ks[5] -= s[8];
+          const float v6[6] = {s[0], s[1], s[2], s[4], s[5], s[8]};
+#pragma unroll
+          for (int t = 0; t < 6; ++t) {
+            const float x = -v6[t];
+            const float sum = Ks[t] + x;
+            const float bp = sum - Ks[t];
+            Kc[t] += (Ks[t] - (sum - bp)) + (x - bp);
+            Ks[t] = sum;
+          }
           Fs[0] += stf[3 * o]; Fs[1] += stf[3 * o + 1]; Fs[2] += stf[3 * o + 2];
         }
         float D[9];
-        finish_row(a, i, Ks, Fs, D);
+        finish_row(a, i, Ks, Kc, Fs, D);
         if (dpos >= 0) {
 #pragma unroll
           for (int t = 0; t < 9; ++t) stv[9 * dpos + t] = D[t];
@@ -399,7 +456,7 @@ assemble_rows(AsmArgs a) {
       // one row longer than the staging: stream it through in pieces
       const int32_t ri = g, i = r0 + ri;
       const RowInfo R = rows[ri];
-      if (threadIdx.x < 9) acc[threadIdx.x] = 0.f;
+      if (threadIdx.x < 9) acc[threadIdx.x] = 0.0;
       int32_t dpos_abs = -1;
       for (int32_t c0 = 0; c0 < nblk; c0 += kAsmCap) {
         const int32_t cn = min(kAsmCap, nblk - c0);
@@ -407,8 +464,9 @@ assemble_rows(AsmArgs a) {
         for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads)
           compute_block(a, i, R, c0 + o, &stv[9 * o], &stf[3 * o], &stc[o], m_valid);
         __syncthreads();
-        // fixed-order partial sums: thread t owns blocks t, t+T, ...
-        float part[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+        // fixed-order fp64 partial sums (one row: the cost is negligible):
+        // thread t owns blocks t, t+T, ...
+        double part[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
         for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads) {
           if (stc[o] == i) { dpos_abs = gob + c0 + o; continue; }
           const float* s = &stv[9 * o];
@@ -418,14 +476,14 @@ assemble_rows(AsmArgs a) {
         }
 #pragma unroll
         for (int q = 0; q < 9; ++q) {
-          float vq = part[q];
+          double vq = part[q];
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) vq += __shfl_down_sync(0xffffffffu, vq, off);
           if ((threadIdx.x & 31) == 0) red[q][threadIdx.x >> 5] = vq;
         }
         __syncthreads();
         if (threadIdx.x < 9) {
-          float s = 0.f;
+          double s = 0.0;
           for (int w = 0; w < kAsmThreads / 32; ++w) s += red[threadIdx.x][w];
           acc[threadIdx.x] += s;
         }
@@ -436,10 +494,15 @@ assemble_rows(AsmArgs a) {
       __syncthreads();
       // the thread that saw the diagonal writes it (exactly one does)
       if (dpos_abs >= 0) {
-        const float Ks[6] = {acc[0], acc[1], acc[2], acc[3], acc[4], acc[5]};
-        const float Fs[3] = {acc[6], acc[7], acc[8]};
+        float Ks[6], Kc[6];
+#pragma unroll
+        for (int t = 0; t < 6; ++t) {   // exact split of the fp64 sum into hi + lo
+          Ks[t] = float(acc[t]);
+          Kc[t] = float(acc[t] - double(Ks[t]));
+        }
+        const float Fs[3] = {float(acc[6]), float(acc[7]), float(acc[8])};
         float D[9];
-        finish_row(a, i, Ks, Fs, D);
+        finish_row(a, i, Ks, Kc, Fs, D);
         float* dst = a.vals + 9 * int64_t(dpos_abs);
 #pragma unroll
         for (int t = 0; t < 9; ++t) dst[t] = D[t];
@@ -450,7 +513,23 @@ assemble_rows(AsmArgs a) {
   }
 }
 
+__global__ void pinv_expand(int32_t n, const float4* __restrict__ p8, float* __restrict__ out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float4 u = p8[2 * i], w = p8[2 * i + 1];
+  float* o = out + 9 * i;
+  o[0] = u.x; o[1] = u.y; o[2] = u.z;
+  o[3] = u.y; o[4] = u.w; o[5] = w.x;
+  o[6] = u.z; o[7] = w.x; o[8] = w.y;
+}
+
 }  // namespace
+
+int launch_pinv_expand(Handle* h, float* out9) {
+  pinv_expand<<<(h->n + 255) / 256, 256, 0, h->stream>>>(h->n, h->pinv8, out9);
+  h->launches += 1;
+  return check_launch(h, "pinv expand");
+}
 
 int assemble_system(Handle* h, const float* x, const float* v,
                     const pcloth_springs* contacts, float dt) {
@@ -511,7 +590,7 @@ int assemble_system(Handle* h, const float* x, const float* v,
   a.colind = h->colind;
   a.vals = h->vals;
   a.rhs = h->rhs;
-  a.pinv = h->pinv;
+  a.pinv8 = h->pinv8;
   a.status = h->d_status;
   assemble_rows<<<ntiles, kAsmThreads, 0, s>>>(a);
   h->launches += 1;

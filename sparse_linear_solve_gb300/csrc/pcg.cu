@@ -22,54 +22,51 @@
 
 #include "pcloth_internal.cuh"
 
+
 namespace pcloth_impl {
 namespace {
 
-// Vertex-to-lane mapping of the vector kernels: a warp covers 10 vertices,
-// lanes 3v..3v+2 hold the components of vertex v (lanes 30, 31 idle), so the
-// three components of a vertex are always read before any is written.
-constexpr int kVertsPerWarp = 10;
+// Vector kernels: one thread per vertex on the padded vectors (one float4
+// (x, y, z, 0) per vertex), so every access of a warp is one contiguous,
+// aligned 512-byte transaction; the symmetric block-Jacobi inverse is two
+// float4 per vertex.  Dot products accumulate a vertex's three terms in fp32
+// and everything after that in fp64.
+__device__ __forceinline__ float3 apply_p(float4 u, float4 w, float3 r) {
+  // P = [[u.x u.y u.z] [u.y u.w w.x] [u.z w.x w.y]]
+  return make_float3(fmaf(u.x, r.x, fmaf(u.y, r.y, u.z * r.z)),
+                     fmaf(u.y, r.x, fmaf(u.w, r.y, w.x * r.z)),
+                     fmaf(u.z, r.x, fmaf(w.x, r.y, w.y * r.z)));
+}
 
-__device__ __forceinline__ bool lane_vertex(int64_t wglobal, int lane, int32_t n,
-                                            int64_t& i, int& c) {
-  i = wglobal * kVertsPerWarp + lane / 3;
-  c = lane - 3 * (lane / 3);
-  return lane < 3 * kVertsPerWarp && i < n;
+__device__ __forceinline__ float dot3(float3 a, float3 b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, a.z * b.z));
 }
 
 __global__ void __launch_bounds__(kVecThreads)
-pcg_init(int32_t n, const float* __restrict__ b, const float* __restrict__ pinv,
-         float* __restrict__ r, float* __restrict__ z, float* __restrict__ dv,
-         float* __restrict__ p_old, double* __restrict__ red_rz0,
-         double* __restrict__ red_bb, PcgState* state) {
-  __shared__ double sh[33];
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t(n) + kVertsPerWarp - 1) / kVertsPerWarp;
-  const int64_t wstride = int64_t(gridDim.x) * (kVecThreads / 32);
+pcg_init(int32_t n, const float* __restrict__ b, const float4* __restrict__ pinv8,
+         float4* __restrict__ r, float4* __restrict__ z, float4* __restrict__ dv,
+         float4* __restrict__ p_old, float2* __restrict__ red_rz0,
+         float2* __restrict__ red_bb, PcgState* state) {
+  __shared__ float2 sh[33 * 2];
   float rz = 0.f, bb = 0.f;
-  for (int64_t w = int64_t(blockIdx.x) * (kVecThreads / 32) + (threadIdx.x >> 5); w < nwarps;
-       w += wstride) {
-    int64_t i;
-    int c;
-    if (!lane_vertex(w, lane, n, i, c)) continue;
-    const int64_t e = 3 * i + c;
-    const float* P = pinv + 9 * i + 3 * c;
-    const float b0 = b[3 * i], b1 = b[3 * i + 1], b2 = b[3 * i + 2];
-    const float be = b[e];
-    const float ze = fmaf(P[0], b0, fmaf(P[1], b1, P[2] * b2));
-    r[e] = be;
-    z[e] = ze;
-    dv[e] = 0.f;
-    p_old[e] = 0.f;
-    rz = fmaf(be, ze, rz);
-    bb = fmaf(be, be, bb);
+  for (int64_t i = int64_t(blockIdx.x) * kVecThreads + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * kVecThreads) {
+    const float3 bv = make_float3(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
+    const float3 zv = apply_p(pinv8[2 * i], pinv8[2 * i + 1], bv);
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    r[i] = make_float4(bv.x, bv.y, bv.z, 0.f);
+    z[i] = make_float4(zv.x, zv.y, zv.z, 0.f);
+    dv[i] = zero;
+    p_old[i] = zero;
+    rz += dot3(bv, zv);
+    bb += dot3(bv, bv);
   }
-  const double trz = block_sum<kVecThreads>(double(rz), sh);
-  const double tbb = block_sum<kVecThreads>(double(bb), sh);
+  Dfloat v[2] = {df_of(rz), df_of(bb)};
+  block_sum_df<kVecThreads, 2>(v, sh);
   if (threadIdx.x == 0) {
-    red_rz0[int64_t(blockIdx.x) * kRedSlots + 0] = trz;
-    red_rz0[int64_t(blockIdx.x) * kRedSlots + 1] = tbb;
-    red_bb[int64_t(blockIdx.x) * kRedSlots + 0] = tbb;
+    red_rz0[int64_t(blockIdx.x) * kRedSlots + 0] = df_pack(v[0]);
+    red_rz0[int64_t(blockIdx.x) * kRedSlots + 1] = df_pack(v[1]);
+    red_bb[int64_t(blockIdx.x) * kRedSlots + 0] = df_pack(v[1]);
     if (blockIdx.x == 0) {
       state->done = 0;
       state->iterations = 0;
@@ -79,81 +76,100 @@ pcg_init(int32_t n, const float* __restrict__ b, const float* __restrict__ pinv,
   }
 }
 
-__global__ void __launch_bounds__(kVecThreads)
-pcg_update(int32_t n, int k, const float* __restrict__ p, const float* __restrict__ q,
-           const float* __restrict__ pinv, float* __restrict__ r, float* __restrict__ z,
-           float* __restrict__ dv, const double* __restrict__ red_pq, int npq,
-           const double* __restrict__ red_rz, const double* __restrict__ red_bb, int nrz,
-           double* __restrict__ red_out, PcgState* state, uint32_t* status) {
-  __shared__ double sh[33];
-  __shared__ int done_sh;
-  if (threadIdx.x == 0) done_sh = state->done;
+// dv += alpha p; r -= alpha q; z = P r; partials of r.z and r.r.  The first
+// vertex's loads are issued before alpha is known, so their latency
+// overlaps the reduction of the previous kernels' partials.
+__global__ void __launch_bounds__(kVecThreads, 4)
+pcg_update(int32_t n, int k, const float4* __restrict__ p, const float4* __restrict__ q,
+           const float4* __restrict__ pinv8, float4* __restrict__ r, float4* __restrict__ z,
+           float4* __restrict__ dv, const float2* __restrict__ red_pq, int npq,
+           const float2* __restrict__ red_rz, const float2* __restrict__ red_bb, int nrz,
+           float2* __restrict__ red_out, PcgState* state, uint32_t* status) {
+  __shared__ float2 sh[33 * 4];
+  __shared__ int flag_sh;
+  __shared__ float alpha_sh;
+  if (threadIdx.x == 0) flag_sh = state->done;
   __syncthreads();
-  if (done_sh) return;
-  const double pq = reduce_partials<kVecThreads>(red_pq, npq, kRedSlots, 0, sh);
-  const double rz = reduce_partials<kVecThreads>(red_rz, nrz, kRedSlots, 0, sh);
-  if (!(pq > 0.0) || !isfinite(pq) || !isfinite(rz)) {
-    const double rr = reduce_partials<kVecThreads>(red_rz, nrz, kRedSlots, 1, sh);
-    const double bb = reduce_partials<kVecThreads>(red_bb, nrz, kRedSlots, 0, sh);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      const bool fin = isfinite(pq) && isfinite(rz);
-      state->done = 1;
-      state->iterations = k;
-      state->relres = sqrt(rr / bb);
-      state->code = fin ? PCLOTH_ERR_BREAKDOWN : PCLOTH_ERR_NONFINITE;
-      atomicOr(status, fin ? ST_BREAKDOWN : ST_NONFINITE);
-    }
-    return;
+  if (flag_sh) return;
+  const int64_t stride = int64_t(gridDim.x) * kVecThreads;
+  int64_t i = int64_t(blockIdx.x) * kVecThreads + threadIdx.x;
+  float4 pv, qv, rv, dvv, pu, pw;
+  if (i < n) {
+    pv = p[i]; qv = q[i]; rv = r[i]; dvv = dv[i]; pu = pinv8[2 * i]; pw = pinv8[2 * i + 1];
   }
-  const float alpha = float(rz / pq);
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t(n) + kVertsPerWarp - 1) / kVertsPerWarp;
-  const int64_t wstride = int64_t(gridDim.x) * (kVecThreads / 32);
-  float arz = 0.f, arr = 0.f;
-  for (int64_t w = int64_t(blockIdx.x) * (kVecThreads / 32) + (threadIdx.x >> 5); w < nwarps;
-       w += wstride) {
-    int64_t i;
-    int c;
-    const bool on = lane_vertex(w, lane, n, i, c);
-    float r0 = 0.f, r1 = 0.f, r2 = 0.f, re = 0.f, ze = 0.f;
-    if (on) {
-      const int64_t v3 = 3 * i, e = v3 + c;
-      dv[e] = fmaf(alpha, p[e], dv[e]);
-      r0 = fmaf(-alpha, q[v3], r[v3]);
-      r1 = fmaf(-alpha, q[v3 + 1], r[v3 + 1]);
-      r2 = fmaf(-alpha, q[v3 + 2], r[v3 + 2]);
-      re = c == 0 ? r0 : (c == 1 ? r1 : r2);
-      const float* P = pinv + 9 * i + 3 * c;
-      ze = fmaf(P[0], r0, fmaf(P[1], r1, P[2] * r2));
-    }
-    __syncwarp();  // all three lanes of a vertex have read r before any writes it
-    if (on) {
-      const int64_t e = 3 * i + c;
-      r[e] = re;
-      z[e] = ze;
-      arz = fmaf(re, ze, arz);
-      arr = fmaf(re, re, arr);
-    }
-  }
-  const double trz = block_sum<kVecThreads>(double(arz), sh);
-  const double trr = block_sum<kVecThreads>(double(arr), sh);
+  Dfloat v[4];   // p.q, r.z, r.r, b.b
+  v[0] = records_share(red_pq, npq, 0, kVecThreads);
+  v[1] = records_share(red_rz, nrz, 0, kVecThreads);
+  v[2] = records_share(red_rz, nrz, 1, kVecThreads);
+  v[3] = records_share(red_bb, nrz, 0, kVecThreads);
+  block_sum_df<kVecThreads, 4>(v, sh);
   if (threadIdx.x == 0) {
-    red_out[int64_t(blockIdx.x) * kRedSlots + 0] = trz;
-    red_out[int64_t(blockIdx.x) * kRedSlots + 1] = trr;
+    const double pq = df_value(v[0]), rz = df_value(v[1]);
+    int stop = 0;
+    if (!(pq > 0.0) || !isfinite(pq) || !isfinite(rz)) {
+      stop = 1;
+      if (blockIdx.x == 0) {
+        const bool fin = isfinite(pq) && isfinite(rz);
+        state->done = 1;
+        state->iterations = k;
+        state->relres = sqrt(df_value(v[2]) / df_value(v[3]));
+        state->code = fin ? PCLOTH_ERR_BREAKDOWN : PCLOTH_ERR_NONFINITE;
+        atomicOr(status, fin ? ST_BREAKDOWN : ST_NONFINITE);
+      }
+    }
+    alpha_sh = float(rz / pq);
+    flag_sh = stop;
+  }
+  __syncthreads();
+  if (flag_sh) return;
+  const float alpha = alpha_sh;
+  float arz = 0.f, arr = 0.f;
+  while (i < n) {
+    const float3 rn = make_float3(fmaf(-alpha, qv.x, rv.x), fmaf(-alpha, qv.y, rv.y),
+                                  fmaf(-alpha, qv.z, rv.z));
+    const float3 zn = apply_p(pu, pw, rn);
+    dv[i] = make_float4(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
+                        fmaf(alpha, pv.z, dvv.z), 0.f);
+    r[i] = make_float4(rn.x, rn.y, rn.z, 0.f);
+    z[i] = make_float4(zn.x, zn.y, zn.z, 0.f);
+    arz += dot3(rn, zn);
+    arr += dot3(rn, rn);
+    i += stride;
+    if (i < n) {
+      pv = p[i]; qv = q[i]; rv = r[i]; dvv = dv[i]; pu = pinv8[2 * i]; pw = pinv8[2 * i + 1];
+    }
+  }
+  Dfloat o[2] = {df_of(arz), df_of(arr)};
+  block_sum_df<kVecThreads, 2>(o, sh);
+  if (threadIdx.x == 0) {
+    red_out[int64_t(blockIdx.x) * kRedSlots + 0] = df_pack(o[0]);
+    red_out[int64_t(blockIdx.x) * kRedSlots + 1] = df_pack(o[1]);
   }
 }
 
+// dv (padded) -> caller's float[n][3].
+__global__ void unpack_dv(int32_t n, const float4* __restrict__ dv4, float* __restrict__ out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float4 d = dv4[i];
+  out[3 * i] = d.x;
+  out[3 * i + 1] = d.y;
+  out[3 * i + 2] = d.z;
+}
+
 // Closes a solve that used all its iterations (or none).
-__global__ void pcg_finish(int k, double tol2, const double* __restrict__ red_rz,
-                           const double* __restrict__ red_bb, int nrz, PcgState* state) {
-  __shared__ double sh[33];
+__global__ void __launch_bounds__(kVecThreads)
+pcg_finish(int k, double tol2, const float2* __restrict__ red_rz,
+           const float2* __restrict__ red_bb, int nrz, PcgState* state) {
+  __shared__ float2 sh[33 * 2];
   __shared__ int done_sh;
   if (threadIdx.x == 0) done_sh = state->done;
   __syncthreads();
   if (done_sh) return;
-  const double rr = reduce_partials<kVecThreads>(red_rz, nrz, kRedSlots, 1, sh);
-  const double bb = reduce_partials<kVecThreads>(red_bb, nrz, kRedSlots, 0, sh);
+  Dfloat v[2] = {records_share(red_rz, nrz, 1, kVecThreads), records_share(red_bb, nrz, 0, kVecThreads)};
+  block_sum_df<kVecThreads, 2>(v, sh);
   if (threadIdx.x == 0) {
+    const double rr = df_value(v[0]), bb = df_value(v[1]);
     state->done = 1;
     state->iterations = k;
     state->relres = bb > 0.0 ? sqrt(rr / bb) : 0.0;
@@ -186,14 +202,15 @@ int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt
   return check_launch(h, "state update");
 }
 
-int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv, int32_t* iterations,
+int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iterations,
               double* rel_residual) {
   cudaStream_t s = h->stream;
+  float4* dv = h->dv4;  // padded; unpacked into dv_out at the end
   const double tol2 = tol * tol;
   const bool prof = h->prof.on;
   const int vg = h->vec_grid;
   if (prof) cudaEventRecord(h->ev[2], s);
-  pcg_init<<<vg, kVecThreads, 0, s>>>(h->n, h->rhs, h->pinv, h->r, h->z, dv, h->p[1],
+  pcg_init<<<vg, kVecThreads, 0, s>>>(h->n, h->rhs, h->pinv8, h->r4, h->z4, dv, h->p4[1],
                                       h->red_upd[0], h->red_init, h->state);
   h->launches += 1;
   int rc = check_launch(h, "pcg init");
@@ -203,15 +220,18 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv, int32_t* iteratio
   int chunk_id = 0, pending = -1;
   bool done = false;
   const int per = 2 * h->chunk + 1;  // events per chunk slot
+  // Profiling samples the first iteration of every chunk (events around its
+  // two launches), which keeps the event overhead out of the other
+  // iterations; a sample of a chunk enqueued after convergence is skipped.
   auto consume = [&](int slot, int launched) {
-    if (!prof) return;
+    if (!prof || launched <= 0 || h->state_host[slot].done) return;
     cudaEvent_t* ev = h->pev.data() + size_t(slot) * per;
-    for (int j = 0; j < launched; ++j) {
-      float a = 0.f, b = 0.f;
-      if (cudaEventElapsedTime(&a, ev[2 * j], ev[2 * j + 1]) == cudaSuccess)
-        h->prof.spmv_ms += a;
-      if (cudaEventElapsedTime(&b, ev[2 * j + 1], ev[2 * j + 2]) == cudaSuccess)
-        h->prof.update_ms += b;
+    float a = 0.f, b = 0.f;
+    if (cudaEventElapsedTime(&a, ev[0], ev[1]) == cudaSuccess &&
+        cudaEventElapsedTime(&b, ev[1], ev[2]) == cudaSuccess) {
+      h->prof.spmv_ms += a;
+      h->prof.update_ms += b;
+      h->prof.samples += 1;
     }
   };
   int launched_in[2] = {0, 0};
@@ -223,13 +243,13 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv, int32_t* iteratio
       if (prof && j == 0) cudaEventRecord(ev[0], s);
       rc = launch_spmv_pcg(h, k, tol);
       if (rc != PCLOTH_OK) return rc;
-      if (prof) cudaEventRecord(ev[2 * j + 1], s);
-      pcg_update<<<vg, kVecThreads, 0, s>>>(h->n, k, h->p[k & 1], h->q, h->pinv, h->r, h->z, dv,
+      if (prof && j == 0) cudaEventRecord(ev[1], s);
+      pcg_update<<<vg, kVecThreads, 0, s>>>(h->n, k, h->p4[k & 1], h->q4, h->pinv8, h->r4, h->z4, dv,
                                             h->red_spmv, h->spmv_grid, h->red_upd[k & 1],
                                             h->red_init, vg, h->red_upd[(k + 1) & 1], h->state,
                                             h->d_status);
       h->launches += 1;
-      if (prof) cudaEventRecord(ev[2 * j + 2], s);
+      if (prof && j == 0) cudaEventRecord(ev[2], s);
     }
     launched_in[slot] = m;
     rc = check_launch(h, "pcg update");
@@ -253,6 +273,10 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv, int32_t* iteratio
   pcg_finish<<<1, kVecThreads, 0, s>>>(k, tol2, h->red_upd[k & 1], h->red_init, vg, h->state);
   h->launches += 1;
   rc = check_launch(h, "pcg finish");
+  if (rc != PCLOTH_OK) return rc;
+  unpack_dv<<<(h->n + 255) / 256, 256, 0, s>>>(h->n, dv, dv_out);
+  h->launches += 1;
+  rc = check_launch(h, "dv unpack");
   if (rc != PCLOTH_OK) return rc;
   cudaMemcpyAsync(&h->state_host[0], h->state, sizeof(PcgState), cudaMemcpyDeviceToHost, s);
   if (prof) cudaEventRecord(h->ev[3], s);

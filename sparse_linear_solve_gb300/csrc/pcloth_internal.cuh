@@ -46,12 +46,8 @@ constexpr int kAsmRows = 32;      // rows per assembly tile
 constexpr int kAsmCap = 768;      // blocks staged per assembly group
 constexpr int kAsmThreads = 256;
 
-constexpr int kSpmvRows = 64;     // rows per SpMV tile
-constexpr int kSpmvCap = 1024;    // blocks staged per SpMV chunk
-constexpr int kSpmvThreads = 256;
-
 constexpr int kVecThreads = 256;
-constexpr int kRedSlots = 4;      // doubles per partial record
+constexpr int kRedSlots = 2;      // double-float (float2) slots per partial record
 
 // --------------------------------------------------------------- handle ----
 struct Profile {
@@ -59,6 +55,7 @@ struct Profile {
   double assemble_ms = 0, spmv_ms = 0, update_ms = 0, solve_ms = 0;
   int64_t spmv_launches = 0, update_launches = 0, assemble_calls = 0;
   int64_t solves = 0, iterations = 0;
+  int64_t samples = 0;   // PCG iterations whose two launches were timed
 };
 
 struct Handle {
@@ -91,7 +88,7 @@ struct Handle {
   int32_t* colind = nullptr;     // nnzb_cap (+pad)
   float* vals = nullptr;         // nnzb_cap*9 (+pad)
   float* rhs = nullptr;          // 3n
-  float* pinv = nullptr;         // 9n
+  float4* pinv8 = nullptr;       // 2 per vertex: (P00 P01 P02 P11) (P12 P22 0 0)
 
   // per-step contact workspace (capacity 2*max_contacts entries)
   uint64_t* ckey[2] = {nullptr, nullptr};
@@ -118,15 +115,17 @@ struct Handle {
   float* hck = nullptr;
   float* hcr = nullptr;
 
-  // PCG workspace
-  float* dv = nullptr;
-  float* r = nullptr;
-  float* z = nullptr;
-  float* p[2] = {nullptr, nullptr};
-  float* q = nullptr;
-  double* red_spmv = nullptr;      // spmv_grid partials (p.q)
-  double* red_upd[2] = {nullptr, nullptr};  // vec_grid * kRedSlots (r.z, r.r)
-  double* red_init = nullptr;      // vec_grid * kRedSlots (b.b)
+  // PCG workspace: one float4 (x, y, z, 0) per vertex, so that a gather is
+  // one aligned 16-byte load and the vector kernels are fully coalesced
+  float* dv = nullptr;             // float[n][3] scratch (pcloth_step without dv)
+  float4* dv4 = nullptr;
+  float4* r4 = nullptr;
+  float4* z4 = nullptr;
+  float4* p4[2] = {nullptr, nullptr};
+  float4* q4 = nullptr;
+  float2* red_spmv = nullptr;      // spmv_grid records (p.q)
+  float2* red_upd[2] = {nullptr, nullptr};  // vec_grid records (r.z, r.r)
+  float2* red_init = nullptr;      // vec_grid records (b.b)
   PcgState* state = nullptr;       // device
   PcgState* state_host = nullptr;  // pinned, 2 slots
   uint32_t* d_status = nullptr;    // device error bits
@@ -158,8 +157,12 @@ int assemble_system(Handle* h, const float* x, const float* v,
                     const pcloth_springs* contacts, float dt);
 
 // spmv.cu
+int spmv_grid_for(int32_t n, int sm_count);
 int launch_spmv(Handle* h, const float* in, float* out);
 int launch_spmv_pcg(Handle* h, int k, double tol);  // k = 0-based iteration
+
+// assemble.cu: expand the packed symmetric inverses to float[n][3][3]
+int launch_pinv_expand(Handle* h, float* out9);
 
 // pcg.cu
 int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv,
@@ -172,39 +175,63 @@ __device__ __forceinline__ bool finite3(float a, float b, float c) {
   return isfinite(a) && isfinite(b) && isfinite(c);
 }
 
-// Deterministic block-wide sum of one double per thread (fixed tree order).
-template <int THREADS>
-__device__ __forceinline__ double block_sum(double v, double* sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  double t = 0.0;
-  if (warp == 0) {
-    t = (lane < THREADS / 32) ? sh[lane] : 0.0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
-  }
-  __syncthreads();
-  return t;  // valid in thread 0
+// Double-float numbers (value = hi + lo, |lo| <= ulp(hi) / 2) for the PCG
+// reductions.  FP64 arithmetic is slow on this part, so every sum is carried
+// in pairs of fp32 with TwoSum, which keeps ~44 bits; each reduction adds in
+// a fixed order, so all CTAs that reduce the same partials get the same bits.
+struct Dfloat {
+  float hi, lo;
+};
+
+__device__ __forceinline__ Dfloat df_add(Dfloat a, Dfloat b) {
+  const float s = a.hi + b.hi;
+  const float bp = s - a.hi;
+  float e = (a.hi - (s - bp)) + (b.hi - bp);   // exact rounding error of a.hi + b.hi
+  e += a.lo + b.lo;
+  const float hi = s + e;
+  return Dfloat{hi, e - (hi - s)};
 }
 
-// Deterministic sum of `count` partial records (slot `slot` of each) that an
-// earlier kernel wrote; every block computes the same value.  Result is
-// broadcast to all threads through shared memory.
-template <int THREADS>
-__device__ __forceinline__ double reduce_partials(const double* part, int count,
-                                                  int stride, int slot,
-                                                  double* sh) {
-  double v = 0.0;
-  for (int t = threadIdx.x; t < count; t += THREADS) v += part[t * stride + slot];
-  v = block_sum<THREADS>(v, sh);
-  if (threadIdx.x == 0) sh[32] = v;
+__device__ __forceinline__ Dfloat df_of(float x) { return Dfloat{x, 0.f}; }
+__device__ __forceinline__ Dfloat df_of(float2 x) { return Dfloat{x.x, x.y}; }
+__device__ __forceinline__ float2 df_pack(Dfloat x) { return make_float2(x.hi, x.lo); }
+__device__ __forceinline__ double df_value(Dfloat x) { return double(x.hi) + double(x.lo); }
+
+// Block-wide sums of N double-floats per thread: a shuffle tree per warp,
+// then warp 0 adds the warp totals in order; results are broadcast to every
+// thread.  sh must hold 33 * N float2.
+template <int THREADS, int N>
+__device__ __forceinline__ void block_sum_df(Dfloat (&v)[N], float2* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const Dfloat u{__shfl_down_sync(0xffffffffu, v[q].hi, o),
+                     __shfl_down_sync(0xffffffffu, v[q].lo, o)};
+      v[q] = df_add(v[q], u);
+    }
+    if (lane == 0) sh[q * 32 + warp] = df_pack(v[q]);
+  }
   __syncthreads();
-  double r = sh[32];
+  if (warp == 0 && lane < N) {
+    Dfloat t = df_of(sh[lane * 32]);
+    for (int w = 1; w < THREADS / 32; ++w) t = df_add(t, df_of(sh[lane * 32 + w]));
+    sh[32 * N + lane] = df_pack(t);
+  }
   __syncthreads();
-  return r;
+#pragma unroll
+  for (int q = 0; q < N; ++q) v[q] = df_of(sh[32 * N + q]);
+  __syncthreads();
+}
+
+// Adds slot `slot` of `count` partial records (kRedSlots float2 each) that an
+// earlier kernel wrote, this thread's share in index order.
+__device__ __forceinline__ Dfloat records_share(const float2* rec, int count, int slot,
+                                                int threads) {
+  Dfloat a{0.f, 0.f};
+  for (int t = threadIdx.x; t < count; t += threads) a = df_add(a, df_of(rec[t * kRedSlots + slot]));
+  return a;
 }
 #endif
 

@@ -259,13 +259,13 @@ def pcloth_profile_enable(h: int, on: bool = True):
 
 def pcloth_profile_read(h: int, reset: bool = False) -> dict:
     ms = (ctypes.c_double * 4)()
-    cnt = (ctypes.c_int64 * 6)()
+    cnt = (ctypes.c_int64 * 7)()
     rc = lib().pcloth_profile_read(h, ms, cnt, int(bool(reset)))
     if rc != OK:
         _raise(h, rc)
     return dict(assemble_ms=ms[0], spmv_ms=ms[1], update_ms=ms[2], solve_ms=ms[3],
                 assemble_calls=cnt[0], spmv_launches=cnt[1], update_launches=cnt[2],
-                solves=cnt[3], iterations=cnt[4], kernel_launches=cnt[5])
+                solves=cnt[3], iterations=cnt[4], kernel_launches=cnt[5], samples=cnt[6])
 
 
 # ------------------------------------------------------------ convenience --
