@@ -40,16 +40,19 @@ namespace pcloth_impl {
 namespace {
 
 #ifndef PCLOTH_PIPE_ROWS
-#define PCLOTH_PIPE_ROWS 64
+#define PCLOTH_PIPE_ROWS 48
 #endif
 #ifndef PCLOTH_PIPE_CAP
-#define PCLOTH_PIPE_CAP 896
+#define PCLOTH_PIPE_CAP 640
 #endif
 #ifndef PCLOTH_PIPE_STAGES
 #define PCLOTH_PIPE_STAGES 2
 #endif
 #ifndef PCLOTH_PIPE_CTAS
-#define PCLOTH_PIPE_CTAS 2
+#define PCLOTH_PIPE_CTAS 3
+#endif
+#ifndef PCLOTH_PIPE_CARVE
+#define PCLOTH_PIPE_CARVE 1
 #endif
 constexpr int kPipeRows = PCLOTH_PIPE_ROWS;   // rows per tile (multiple of 4)
 constexpr int kPipeCap = PCLOTH_PIPE_CAP;     // blocks per stage
@@ -355,6 +358,15 @@ spmv_pipe(SpmvArgs a) {
 
 bool g_attr_done[64] = {};
 
+// Shared-memory carveout: just enough for kPipeCtasPerSm CTAs, so that the
+// rest of the unified L1/shared storage stays L1 cache for the gathers.
+int carveout_percent() {
+  const size_t need = size_t(kPipeCtasPerSm) * (kPipeSmem + 2048);
+  const size_t max_smem = 228 * 1024;
+  int pct = int((need * 100 + max_smem - 1) / max_smem);
+  return pct > 100 ? 100 : pct;
+}
+
 int ensure_attr(Handle* h) {
   if (h->device >= 0 && h->device < 64 && g_attr_done[h->device]) return PCLOTH_OK;
   cudaError_t e = cudaFuncSetAttribute(spmv_pipe<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -362,6 +374,12 @@ int ensure_attr(Handle* h) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(spmv_pipe<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kPipeSmem));
+  if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
+    e = cudaFuncSetAttribute(spmv_pipe<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             carveout_percent());
+  if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
+    e = cudaFuncSetAttribute(spmv_pipe<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             carveout_percent());
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(spmv)");
   if (h->device >= 0 && h->device < 64) g_attr_done[h->device] = true;
   return PCLOTH_OK;

@@ -112,15 +112,22 @@ def test_contacts_duplicates_and_spring_pairs():
 
 def test_long_rows_exercise_chunked_paths():
     """One vertex in contact with 1500 others: its row is longer than the
-    assembly staging and the SpMV chunk, and a tile exceeds both."""
+    assembly staging and the SpMV chunk, and a tile exceeds both.
+
+    The contacts are soft (k in [1, 10]) and near their rest lengths: with
+    contact stiffness 1e3 from one vertex to most of the cloth, the hub's
+    diagonal block reaches ~1e6 times its mass, and fp32 storage of that one
+    block alone moves the exact solution by ~2e-5; this test is about the
+    long-row code paths, not about that conditioning."""
     w = W.tiny_cloth(n=48, rest_from_grid=True)
     N = w.n_verts
     hub = N // 2 + 7
     others = np.array([j for j in range(N) if j != hub][:1500], np.int32)
     rng = np.random.default_rng(5)
+    dist = np.linalg.norm(w.x0[others].astype(np.float64) - w.x0[hub], axis=1)
     c = W.Contacts(np.full(len(others), hub, np.int32), others,
-                   rng.uniform(1e2, 1e3, len(others)).astype(np.float32),
-                   rng.uniform(1e-3, 5e-2, len(others)).astype(np.float32))
+                   rng.uniform(1.0, 10.0, len(others)).astype(np.float32),
+                   (dist * rng.uniform(0.9, 1.1, len(others))).astype(np.float32))
     w.max_contacts = len(others)
     pcl, ref, g, _ = compare_assembly(w, w.x0, w.v0, c)
     assert int(g["rowptr"][hub + 1] - g["rowptr"][hub]) > 1024
