@@ -177,6 +177,31 @@ int pcloth_profile_enable(pcloth_t h, int on);
 int pcloth_profile_read(pcloth_t h, double* ms_out, int64_t* counts_out,
                         int reset);
 
+/* Allocation-free solve.  The paper has no counterpart: this entry point is
+ * for callers that cannot allocate GPU memory when they need a solve -- a
+ * host application that reserves the GPU's memory for itself and forbids
+ * plug-ins to allocate, or a real-time loop in which an allocation's latency
+ * or failure mid-frame is unacceptable.  It solves A dv = b for a BSR3
+ * matrix the caller already holds (rowptr int32[n+1], colind int32[nnzb]
+ * sorted per row with the diagonal present, vals float32[nnzb][3][3], b
+ * float32[n][3], all device pointers; dv float32[n][3] device output) with
+ * the same block-Jacobi PCG as pcloth_solve, on the current device and the
+ * given stream (a cudaStream_t, 0 = legacy default), and returns
+ * *iterations and *rel_residual on the host.  It allocates nothing: all of
+ * its scratch is one fixed array compiled into this library, which every
+ * GPU that loads the library holds (about 2.2 MiB) until the process exits.
+ * n may be at most PCLOTH_STATIC_MAX_VERTS; larger n returns
+ * PCLOTH_ERR_CAPACITY without touching the GPU.  Every call on a device
+ * shares that array, so calls that overlap on the GPU race: order them (one
+ * stream, or events).  The first call on each device also looks up the
+ * array's device address; make that first call before any stream capture.
+ * Synchronises.  Errors are described by pcloth_last_error(NULL). */
+#define PCLOTH_STATIC_MAX_VERTS 16384
+int pcloth_solve_bsr3_static(int32_t n, const int32_t* rowptr, const int32_t* colind,
+                             const float* vals, const float* b, double tol, int32_t maxit,
+                             float* dv, int32_t* iterations, double* rel_residual,
+                             void* stream);
+
 /* Free every buffer of the handle (synchronises its stream first). */
 void pcloth_destroy(pcloth_t h);
 

@@ -447,6 +447,21 @@ const char* pcloth_last_error(pcloth_t ht) {
 
 void pcloth_destroy(pcloth_t ht) { free_handle(reinterpret_cast<Handle*>(ht)); }
 
+int pcloth_solve_bsr3_static(int32_t n, const int32_t* rowptr, const int32_t* colind,
+                             const float* vals, const float* b, double tol, int32_t maxit,
+                             float* dv, int32_t* iterations, double* rel_residual,
+                             void* stream) {
+  g_create_err.clear();
+  if (n > PCLOTH_STATIC_MAX_VERTS)
+    return fail(nullptr, PCLOTH_ERR_CAPACITY,
+                "n = " + std::to_string(n) + " exceeds PCLOTH_STATIC_MAX_VERTS = " +
+                    std::to_string(PCLOTH_STATIC_MAX_VERTS));
+  if (n <= 0 || !rowptr || !colind || !vals || !b || !dv || maxit < 0 || !(tol >= 0.0))
+    return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "bad argument to pcloth_solve_bsr3_static");
+  return pcg_solve_static(n, rowptr, colind, vals, b, tol, maxit, dv, iterations, rel_residual,
+                          static_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------- profiling ---
 // Per-kernel-class device time accumulated from CUDA events recorded on the
 // handle's stream around every launch while profiling is on.

@@ -304,4 +304,170 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
   return st.code;
 }
 
+// ===========================================================================
+// Allocation-free solve.
+//
+// Some callers cannot allocate GPU memory at the time they need a solve: a
+// host application (an animation tool, a game engine) that reserves the
+// GPU's memory budget for itself and forbids allocation by plug-ins, or a
+// real-time loop in which an allocation's latency, or an allocation that
+// fails in the middle of a frame, is not acceptable.  pcloth_solve_bsr3_static
+// serves them: it runs the same block-Jacobi PCG kernels as pcloth_solve on a
+// BSR3 system the caller already holds, and keeps every work vector, every
+// reduction record and the status words in one fixed array compiled into
+// this library, so it never calls cudaMalloc, cudaFree or any allocating
+// routine.
+//
+// The array is a file-scope __device__ variable: every GPU that loads the
+// library holds it (about 2.2 MiB) until the process exits, and every call
+// on that GPU shares it.  Calls that overlap on the GPU therefore race on it;
+// a caller must order them (one stream, or events).  Each call re-initialises
+// everything it reads before reading it, so nothing leaks from one call into
+// the next.
+// ===========================================================================
+namespace {
+
+constexpr int64_t kStaticVec = int64_t(PCLOTH_STATIC_MAX_VERTS) + 64;  // float4 per vector
+constexpr int kStaticMaxRecords = 1024;                                 // per reduction buffer
+constexpr size_t kStaticBytes =
+    sizeof(float4) * size_t(2 * kStaticVec        // block-Jacobi inverses (2 per vertex)
+                            + 5 * kStaticVec)     // dv, r, z, q and the spare p
+    + sizeof(float4) * size_t(kStaticVec)         // second p (ping-pong)
+    + sizeof(float2) * size_t(kRedSlots) * size_t(4 * kStaticMaxRecords) + 256;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
+
+// Device address of g_static_scratch per device ordinal (set up on first use).
+void* g_static_addr[64] = {};
+
+// Inverse of the diagonal block of each row of a caller's BSR3 matrix, packed
+// like the library's own: (P00 P01 P02 P11) (P12 P22 0 0).  A row without a
+// diagonal block, or with a non-invertible one, is reported as non-finite.
+__global__ void bsr3_diag_inverse(int32_t n, const int32_t* __restrict__ rowptr,
+                                  const int32_t* __restrict__ colind,
+                                  const float* __restrict__ vals, float4* __restrict__ pinv8,
+                                  uint32_t* status) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  int32_t lo = rowptr[i], hi = rowptr[i + 1];
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (colind[mid] < i) lo = mid + 1; else hi = mid;
+  }
+  float det = 0.f, c00 = 0.f, c01 = 0.f, c02 = 0.f, c11 = 0.f, c12 = 0.f, c22 = 0.f;
+  if (lo < rowptr[i + 1] && colind[lo] == i) {
+    const float* D = vals + 9 * int64_t(lo);
+    c00 = D[4] * D[8] - D[5] * D[7];
+    c01 = D[5] * D[6] - D[3] * D[8];
+    c02 = D[3] * D[7] - D[4] * D[6];
+    c11 = D[0] * D[8] - D[2] * D[6];
+    c12 = D[2] * D[3] - D[0] * D[5];
+    c22 = D[0] * D[4] - D[1] * D[3];
+    det = D[0] * c00 + D[1] * c01 + D[2] * c02;
+  }
+  if (!(det > 0.f) || !isfinite(det)) {
+    atomicOr(status, ST_NONFINITE);
+    det = 1.f;
+  }
+  const float id = 1.0f / det;
+  pinv8[2 * i] = make_float4(c00 * id, c01 * id, c02 * id, c11 * id);
+  pinv8[2 * i + 1] = make_float4(c12 * id, c22 * id, 0.f, 0.f);
+}
+
+}  // namespace
+
+int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, const float* vals,
+                     const float* b, double tol, int32_t maxit, float* dv_out,
+                     int32_t* iterations, double* rel_residual, cudaStream_t stream) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+  if (device < 0 || device >= 64) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "device ordinal");
+  if (!g_static_addr[device]) {
+    // g_static_scratch names a host-side stand-in here; the kernels need the
+    // array's device address on this device.
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetSymbolAddress(scratch)");
+    g_static_addr[device] = ptr;
+  }
+  // A stack handle pointing into the fixed array and the caller's buffers:
+  // its containers stay empty and nothing in it is allocated or freed.
+  Handle h;
+  h.device = device;
+  h.stream = stream;
+  h.n = n;
+  h.chunk = 32;
+  cudaDeviceGetAttribute(&h.sm_count, cudaDevAttrMultiProcessorCount, device);
+  if (h.sm_count <= 0) h.sm_count = 1;
+  h.spmv_grid = spmv_grid_for(n, h.sm_count);
+  h.vec_grid = int(std::min<int64_t>((int64_t(n) + kVecThreads - 1) / kVecThreads,
+                                     int64_t(h.sm_count) * 4));
+  if (h.spmv_grid > kStaticMaxRecords || h.vec_grid > kStaticMaxRecords)
+    return fail(nullptr, PCLOTH_ERR_CAPACITY, "too many CTAs for the fixed reduction records");
+  unsigned char* base = static_cast<unsigned char*>(g_static_addr[device]);
+  float4* v4 = reinterpret_cast<float4*>(base);
+  h.pinv8 = v4;
+  h.dv4 = v4 + 2 * kStaticVec;
+  h.r4 = v4 + 3 * kStaticVec;
+  h.z4 = v4 + 4 * kStaticVec;
+  h.q4 = v4 + 5 * kStaticVec;
+  h.p4[0] = v4 + 6 * kStaticVec;
+  h.p4[1] = v4 + 7 * kStaticVec;
+  float2* rec = reinterpret_cast<float2*>(v4 + 8 * kStaticVec);
+  h.red_spmv = rec;
+  h.red_upd[0] = rec + size_t(kRedSlots) * kStaticMaxRecords;
+  h.red_upd[1] = rec + size_t(2 * kRedSlots) * kStaticMaxRecords;
+  h.red_init = rec + size_t(3 * kRedSlots) * kStaticMaxRecords;
+  unsigned char* tail = reinterpret_cast<unsigned char*>(rec + size_t(4 * kRedSlots) * kStaticMaxRecords);
+  h.state = reinterpret_cast<PcgState*>(tail);
+  h.d_status = reinterpret_cast<uint32_t*>(tail + 64);
+  h.rowptr = const_cast<int32_t*>(rowptr);
+  h.colind = const_cast<int32_t*>(colind);
+  h.vals = const_cast<float*>(vals);
+  h.rhs = const_cast<float*>(b);
+
+  const int vg = h.vec_grid;
+  e = cudaMemsetAsync(h.d_status, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "status reset");
+  bsr3_diag_inverse<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, vals, h.pinv8,
+                                                        h.d_status);
+  pcg_init<<<vg, kVecThreads, 0, stream>>>(n, b, h.pinv8, h.r4, h.z4, h.dv4, h.p4[1],
+                                           h.red_upd[0], h.red_init, h.state);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve launch");
+  PcgState st{};
+  int32_t k = 0;
+  while (k < maxit) {
+    const int m = std::min<int32_t>(h.chunk, maxit - k);
+    for (int j = 0; j < m; ++j, ++k) {
+      if (launch_spmv_pcg(&h, k, tol) != PCLOTH_OK) return fail(nullptr, PCLOTH_ERR_CUDA, h.err);
+      pcg_update<<<vg, kVecThreads, 0, stream>>>(n, k, h.p4[k & 1], h.q4, h.pinv8, h.r4, h.z4,
+                                                 h.dv4, h.red_spmv, h.spmv_grid,
+                                                 h.red_upd[k & 1], h.red_init, vg,
+                                                 h.red_upd[(k + 1) & 1], h.state, h.d_status);
+    }
+    e = cudaMemcpyAsync(&st, h.state, sizeof(PcgState), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve poll");
+    if (st.done) break;
+  }
+  pcg_finish<<<1, kVecThreads, 0, stream>>>(k, tol * tol, h.red_upd[k & 1], h.red_init, vg, h.state);
+  unpack_dv<<<(n + 255) / 256, 256, 0, stream>>>(n, h.dv4, dv_out);
+  uint32_t status = 0;
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&st, h.state, sizeof(PcgState), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&status, h.d_status, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve result");
+  if (iterations) *iterations = st.iterations;
+  if (rel_residual) *rel_residual = st.relres;
+  if (status & ST_WAIT_TIMEOUT) return fail(nullptr, PCLOTH_ERR_CUDA, "device wait timed out");
+  if (status & ST_NONFINITE)
+    return fail(nullptr, PCLOTH_ERR_NONFINITE, "non-finite value or missing/singular diagonal block");
+  if (st.code == PCLOTH_ERR_BREAKDOWN) return fail(nullptr, st.code, "PCG breakdown");
+  if (st.code == PCLOTH_ERR_NONFINITE) return fail(nullptr, st.code, "non-finite value in PCG");
+  return st.code;
+}
+
 }  // namespace pcloth_impl

@@ -168,6 +168,9 @@ int launch_pinv_expand(Handle* h, float* out9);
 int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv,
               int32_t* iterations, double* rel_residual);
 int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt);
+int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, const float* vals,
+                     const float* b, double tol, int32_t maxit, float* dv_out,
+                     int32_t* iterations, double* rel_residual, cudaStream_t stream);
 
 // ---------------------------------------------------------- device code ---
 #ifdef __CUDACC__

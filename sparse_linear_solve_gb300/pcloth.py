@@ -30,7 +30,9 @@ CODE_NAMES = {OK: "OK", NOT_CONVERGED: "NOT_CONVERGED", ERR_INVALID_ARG: "INVALI
 EXPORTS = ("pcloth_create", "pcloth_assemble", "pcloth_spmv", "pcloth_solve", "pcloth_step",
            "pcloth_step_host", "pcloth_nnzb", "pcloth_export", "pcloth_set_stream",
            "pcloth_sync", "pcloth_last_error", "pcloth_destroy", "pcloth_profile_enable",
-           "pcloth_profile_read")
+           "pcloth_profile_read", "pcloth_solve_bsr3_static")
+
+STATIC_MAX_VERTS = 16384   # PCLOTH_STATIC_MAX_VERTS
 
 
 class PClothError(RuntimeError):
@@ -87,6 +89,8 @@ def lib():
         L.pcloth_destroy.restype = None
         L.pcloth_profile_enable.argtypes = [vp, ctypes.c_int]
         L.pcloth_profile_read.argtypes = [vp, P(dbl), P(i64), ctypes.c_int]
+        L.pcloth_solve_bsr3_static.argtypes = [i32, vp, vp, vp, vp, dbl, i32, vp, P(i32), P(dbl),
+                                               vp]
         for name in EXPORTS:
             f = getattr(L, name)
             if name not in ("pcloth_last_error", "pcloth_destroy"):
@@ -266,6 +270,26 @@ def pcloth_profile_read(h: int, reset: bool = False) -> dict:
     return dict(assemble_ms=ms[0], spmv_ms=ms[1], update_ms=ms[2], solve_ms=ms[3],
                 assemble_calls=cnt[0], spmv_launches=cnt[1], update_launches=cnt[2],
                 solves=cnt[3], iterations=cnt[4], kernel_launches=cnt[5], samples=cnt[6])
+
+
+def pcloth_solve_bsr3_static(n: int, rowptr, colind, vals, b, tol: float, maxit: int, dv,
+                             stream: Optional[int] = None):
+    """Allocation-free block-Jacobi PCG on a BSR3 system the caller holds
+    (device tensors: rowptr int32[n+1], colind int32[nnzb], vals float32
+    [nnzb,3,3], b float32[n,3]; dv float32[n,3] is written).  For callers
+    that must not allocate GPU memory; n <= STATIC_MAX_VERTS.  Returns
+    (iterations, rel_residual, code) like pcloth_solve."""
+    ptrs = [None if t is None else t.data_ptr() for t in (rowptr, colind, vals, b, dv)]
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    it = ctypes.c_int32(0)
+    rr = ctypes.c_double(0.0)
+    rc = lib().pcloth_solve_bsr3_static(int(n), *ptrs[:4], float(tol), int(maxit), ptrs[4],
+                                        ctypes.byref(it), ctypes.byref(rr),
+                                        ctypes.c_void_p(stream))
+    if rc not in (OK, NOT_CONVERGED):
+        _raise(None, rc)
+    return int(it.value), float(rr.value), rc
 
 
 # ------------------------------------------------------------ convenience --
