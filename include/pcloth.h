@@ -166,8 +166,8 @@ const char* pcloth_last_error(pcloth_t h);
 
 /* Profiling: while enabled, the library records CUDA events on its stream
  * around every assembly and solve, and around the two launches (SpMV, PCG
- * update) of the first iteration of every polling chunk, and accumulates
- * their device time.  pcloth_profile_read fills ms_out[4] = {assembly,
+ * update) of the first iteration of every polling chunk (on = 1) or of every
+ * iteration (on = 2), and accumulates their device time.  pcloth_profile_read fills ms_out[4] = {assembly,
  * sampled PCG SpMV, sampled PCG update, whole solves} in milliseconds and
  * counts_out[7] = {assemblies, SpMV launches, update launches, solves, PCG
  * iterations, kernels launched by this handle, sampled iterations}; divide

@@ -469,6 +469,7 @@ int pcloth_profile_enable(pcloth_t ht, int on) {
   Handle* h = reinterpret_cast<Handle*>(ht);
   if (!h) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "NULL handle");
   h->prof.on = on != 0;
+  h->prof.mode = on == 2 ? 2 : 1;
   return PCLOTH_OK;
 }
 
@@ -491,9 +492,11 @@ int pcloth_profile_read(pcloth_t ht, double* ms_out, int64_t* counts_out, int re
     counts_out[6] = h->prof.samples;
   }
   if (reset) {
-    bool on = h->prof.on;
+    const bool on = h->prof.on;
+    const int mode = h->prof.mode;
     h->prof = Profile();
     h->prof.on = on;
+    h->prof.mode = mode;
     h->launches = 0;
   }
   return PCLOTH_OK;

@@ -218,20 +218,27 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
 
   int32_t k = 0;
   int chunk_id = 0, pending = -1;
+  h->prof_done_at = INT32_MAX;
   bool done = false;
   const int per = 2 * h->chunk + 1;  // events per chunk slot
-  // Profiling samples the first iteration of every chunk (events around its
-  // two launches), which keeps the event overhead out of the other
-  // iterations; a sample of a chunk enqueued after convergence is skipped.
+  // Profiling mode 1 times the first iteration of every chunk (events around
+  // its two launches); mode 2 times every iteration.  Iterations enqueued
+  // after convergence return at once and are not counted.
+  const bool every = h->prof.mode == 2;
   auto consume = [&](int slot, int launched) {
-    if (!prof || launched <= 0 || h->state_host[slot].done) return;
+    if (!prof || launched <= 0) return;
     cudaEvent_t* ev = h->pev.data() + size_t(slot) * per;
-    float a = 0.f, b = 0.f;
-    if (cudaEventElapsedTime(&a, ev[0], ev[1]) == cudaSuccess &&
-        cudaEventElapsedTime(&b, ev[1], ev[2]) == cudaSuccess) {
-      h->prof.spmv_ms += a;
-      h->prof.update_ms += b;
-      h->prof.samples += 1;
+    const int timed = every ? launched : 1;
+    const int32_t first_k = h->prof_chunk_k[slot];
+    for (int j = 0; j < timed; ++j) {
+      if (first_k + j >= h->prof_done_at) break;   // launches from here on were no-ops
+      float a = 0.f, b = 0.f;
+      if (cudaEventElapsedTime(&a, ev[2 * j], ev[2 * j + 1]) == cudaSuccess &&
+          cudaEventElapsedTime(&b, ev[2 * j + 1], ev[2 * j + 2]) == cudaSuccess) {
+        h->prof.spmv_ms += a;
+        h->prof.update_ms += b;
+        h->prof.samples += 1;
+      }
     }
   };
   int launched_in[2] = {0, 0};
@@ -239,17 +246,19 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
     const int slot = chunk_id & 1;
     const int m = std::min<int32_t>(h->chunk, maxit - k);
     cudaEvent_t* ev = h->pev.data() + size_t(slot) * per;
+    h->prof_chunk_k[slot] = k;
     for (int j = 0; j < m; ++j, ++k) {
-      if (prof && j == 0) cudaEventRecord(ev[0], s);
+      const bool rec = prof && (every || j == 0);
+      if (rec && j == 0) cudaEventRecord(ev[0], s);
       rc = launch_spmv_pcg(h, k, tol);
       if (rc != PCLOTH_OK) return rc;
-      if (prof && j == 0) cudaEventRecord(ev[1], s);
+      if (rec) cudaEventRecord(ev[2 * j + 1], s);
       pcg_update<<<vg, kVecThreads, 0, s>>>(h->n, k, h->p4[k & 1], h->q4, h->pinv8, h->r4, h->z4, dv,
                                             h->red_spmv, h->spmv_grid, h->red_upd[k & 1],
                                             h->red_init, vg, h->red_upd[(k + 1) & 1], h->state,
                                             h->d_status);
       h->launches += 1;
-      if (prof && j == 0) cudaEventRecord(ev[2], s);
+      if (rec) cudaEventRecord(ev[2 * j + 2], s);
     }
     launched_in[slot] = m;
     rc = check_launch(h, "pcg update");
@@ -259,8 +268,11 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
     if (pending >= 0) {
       cudaError_t e = cudaEventSynchronize(h->chunk_ev[pending]);
       if (e != cudaSuccess) return cuda_fail(h, e, "pcg poll");
+      if (h->state_host[pending].done) {
+        done = true;
+        h->prof_done_at = h->state_host[pending].iterations;
+      }
       consume(pending, launched_in[pending]);
-      if (h->state_host[pending].done) done = true;
     }
     pending = slot;
     ++chunk_id;
@@ -268,6 +280,8 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
   if (pending >= 0) {
     cudaError_t e = cudaEventSynchronize(h->chunk_ev[pending]);
     if (e != cudaSuccess) return cuda_fail(h, e, "pcg poll");
+    if (h->state_host[pending].done && h->prof_done_at > h->state_host[pending].iterations)
+      h->prof_done_at = h->state_host[pending].iterations;
     consume(pending, launched_in[pending]);
   }
   pcg_finish<<<1, kVecThreads, 0, s>>>(k, tol2, h->red_upd[k & 1], h->red_init, vg, h->state);

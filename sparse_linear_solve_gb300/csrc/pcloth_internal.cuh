@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
+
 #include <string>
 #include <vector>
 
@@ -52,6 +54,7 @@ constexpr int kRedSlots = 2;      // double-float (float2) slots per partial rec
 // --------------------------------------------------------------- handle ----
 struct Profile {
   bool on = false;
+  int mode = 1;          // 1: first iteration of each chunk, 2: every iteration
   double assemble_ms = 0, spmv_ms = 0, update_ms = 0, solve_ms = 0;
   int64_t spmv_launches = 0, update_launches = 0, assemble_calls = 0;
   int64_t solves = 0, iterations = 0;
@@ -136,6 +139,8 @@ struct Handle {
   cudaEvent_t ev[8] = {};
   std::vector<cudaEvent_t> pev;   // per-launch events of two PCG chunks
   cudaEvent_t chunk_ev[2] = {};
+  int32_t prof_chunk_k[2] = {0, 0};  // first iteration of the chunk in each slot
+  int32_t prof_done_at = 0;          // iterations that did work, once known
 };
 
 // ------------------------------------------------------------- helpers ----

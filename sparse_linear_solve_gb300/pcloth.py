@@ -255,8 +255,9 @@ def pcloth_destroy(h: int):
     lib().pcloth_destroy(h)
 
 
-def pcloth_profile_enable(h: int, on: bool = True):
-    rc = lib().pcloth_profile_enable(h, int(bool(on)))
+def pcloth_profile_enable(h: int, on=True):
+    """on: 0/False off, 1/True sample one iteration per chunk, 2 every iteration."""
+    rc = lib().pcloth_profile_enable(h, int(on))
     if rc != OK:
         _raise(h, rc)
 
@@ -394,7 +395,7 @@ class PCloth:
         pcloth_export(self.h, out["rowptr"], out["colind"], out["vals"], out["b"], out["pinv"])
         return out
 
-    def profile(self, on: bool = True):
+    def profile(self, on=True):
         pcloth_profile_enable(self.h, on)
 
     def profile_read(self, reset: bool = False) -> dict:

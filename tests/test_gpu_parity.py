@@ -261,3 +261,24 @@ def test_chunk_size_does_not_change_results():
         res.append((dv.cpu().numpy(), it, rr))
     for r in res[1:]:
         assert np.array_equal(r[0], res[0][0]) and r[1] == res[0][1] and r[2] == res[0][2]
+
+
+def test_profiling_modes_count_the_iterations_they_time():
+    """Mode 2 times both launches of every iteration that did work; mode 1
+    the first iteration of each chunk.  Resetting the counters keeps the
+    mode.  Profiling changes no result."""
+    w = W.drooped_cloth(n=30)
+    ref_pcl = make(w, chunk=8)
+    xr, vr = to_dev(w.x0), to_dev(w.v0)
+    it_ref, rr_ref, _ = ref_pcl.step(xr, vr, None, w.h, w.tol, w.maxit)
+    for mode, expect in ((2, lambda it: it), (1, lambda it: -(-it // 8))):
+        pcl = make(w, chunk=8)
+        pcl.profile(mode)
+        pcl.profile_read(reset=True)
+        xd, vd = to_dev(w.x0), to_dev(w.v0)
+        it, rr, _ = pcl.step(xd, vd, None, w.h, w.tol, w.maxit)
+        p = pcl.profile_read(reset=True)
+        assert it == it_ref and rr == rr_ref
+        assert torch.equal(xd, xr) and torch.equal(vd, vr)
+        assert p["iterations"] == it and p["samples"] == expect(it), (mode, p, it)
+        assert p["spmv_ms"] > 0 and p["update_ms"] > 0 and p["assemble_calls"] == 1
