@@ -246,7 +246,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- roofline of the dominant kernel: the PCG SpMV -------------------
     n = w.n_verts
     nnzb = nnzb_seen[-1]
-    bytes_per_launch = 40 * nnzb + 52 * n
+    bytes_per_launch = 28 * nnzb + 52 * n
     samples = max(prof["samples"], 1)
     spmv_avg_ms = prof["spmv_ms"] / samples
     achieved = bytes_per_launch / (spmv_avg_ms * 1e-3) / 1e9
@@ -293,7 +293,7 @@ def run_ours(args, rank, world, local_rank):
         data="synthetic (seeded generator; no garment meshes available)",
         config=dict(workload_desc(w), parallelism="replicas only (one independent cloth per GPU)",
                     l2="inputs larger than L2: A is %.0f MB per step vs 129 MB L2" %
-                    (nnzb * 40 / 1e6)),
+                    (nnzb * 28 / 1e6)),
         pcg_iterations_per_s=whole_job_rate(world, sum(its), ms * 1e-3),
         pcg_iterations_per_s_solve_only=sum(its_prof) / (prof["solve_ms"] * 1e-3),
         pcg_iterations_mean=sum(its) / K,
@@ -309,7 +309,7 @@ def run_ours(args, rank, world, local_rank):
                              "with the events)" % (K, prof["samples"], ms_prof / K),
                       achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
                       peak_source=peak_src, bytes_per_launch=bytes_per_launch,
-                      bytes_model="40 B/block (36 values + 4 colind) + 52 B/row (rowptr 4, "
+                      bytes_model="28 B/block (24 packed symmetric values + 4 colind) + 52 B/row (rowptr 4, "
                                   "z 12, p_old 12 read; p 12, q 12 written)",
                       traffic=stored_traffic(spmv_source_digest())),
         clocks=clk,

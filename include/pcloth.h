@@ -23,8 +23,12 @@
  *
  * Storage (all on the device, owned by the library unless noted):
  *   matrix     BSR3: rowptr int32[n+1], colind int32[nnzb] (sorted per row,
- *              unique, diagonal always present), vals float32[nnzb][3][3]
- *              (row-major blocks, rows consecutive);
+ *              unique, diagonal always present), block values with rows
+ *              consecutive.  Every block of A is symmetric (a sum of the
+ *              symmetric K_e, plus m_i I on the diagonal), so the library
+ *              holds each packed as six floats (a00 a01 a02 a11 a12 a22),
+ *              float32[nnzb][6]; pcloth_export expands them to row-major
+ *              float32[nnzb][3][3];
  *   vectors    float32[n][3] (x, y, z interleaved per vertex).
  * The pattern of the springs is built once by pcloth_create; every
  * pcloth_assemble merges that step's contact pairs into it in place, inside
@@ -149,8 +153,11 @@ int pcloth_step_host(pcloth_t h, float* x, float* v,
 int pcloth_nnzb(pcloth_t h, int64_t* nnzb);
 
 /* Copy the last assembled system into caller-owned device buffers (any may
- * be NULL): rowptr int32[n+1], colind int32[nnzb], vals float32[nnzb*9],
- * b float32[n*3], pinv float32[n*9].  Synchronises. */
+ * be NULL): rowptr int32[n+1], colind int32[nnzb], vals float32[nnzb*9]
+ * (row-major 3x3 blocks, expanded from the packed symmetric storage), b
+ * float32[n*3], pinv float32[n*9] (the block-Jacobi inverses, row-major).
+ * vals and pinv must be device memory (a kernel writes them).
+ * Synchronises. */
 int pcloth_export(pcloth_t h, int32_t* rowptr, int32_t* colind, float* vals,
                   float* b, float* pinv);
 
@@ -167,12 +174,14 @@ const char* pcloth_last_error(pcloth_t h);
 /* Profiling: while enabled, the library records CUDA events on its stream
  * around every assembly and solve, and around the two launches (SpMV, PCG
  * update) of the first iteration of every polling chunk (on = 1) or of every
- * iteration (on = 2), and accumulates their device time.  pcloth_profile_read fills ms_out[4] = {assembly,
- * sampled PCG SpMV, sampled PCG update, whole solves} in milliseconds and
- * counts_out[7] = {assemblies, SpMV launches, update launches, solves, PCG
- * iterations, kernels launched by this handle, sampled iterations}; divide
- * the sampled times by the sample count for a per-launch average.
- * reset != 0 zeroes the accumulators. */
+ * iteration (on = 2), and accumulates their device time; on = 0 disables.
+ * Iterations launched after convergence (they return at once) are not
+ * sampled.  pcloth_profile_read fills ms_out[4] = {assembly, sampled PCG
+ * SpMV, sampled PCG update, whole solves} in milliseconds and counts_out[7] =
+ * {assemblies, SpMV launches, update launches, solves, PCG iterations,
+ * kernels launched by this handle, sampled iterations}; divide the sampled
+ * times by the sample count for a per-launch average.  reset != 0 zeroes the
+ * accumulators and keeps the profiling mode. */
 int pcloth_profile_enable(pcloth_t h, int on);
 int pcloth_profile_read(pcloth_t h, double* ms_out, int64_t* counts_out,
                         int reset);

@@ -222,7 +222,7 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->sentry, std::max<int64_t>(2 * ns, 1)));
   A(dalloc(&h->rowptr, n + 1 + vpad));
   A(dalloc(&h->colind, cap + vpad));
-  A(dalloc(&h->vals, cap * 9 + vpad));
+  A(dalloc(&h->vals, cap * kSymBlock + vpad));
   A(dalloc(&h->rhs, 3 * n + vpad));
   A(dalloc(&h->pinv8, 2 * n + vpad));
   for (int b = 0; b < 2; ++b) {
@@ -274,7 +274,7 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   if (e == cudaSuccess && !sentry.empty())
     e = cudaMemcpy(h->sentry, sentry.data(), sentry.size() * sizeof(float2), cudaMemcpyHostToDevice);
   // zero the padding and workspaces so that no read ever sees garbage
-  if (e == cudaSuccess) e = cudaMemset(h->vals, 0, (cap * 9 + vpad) * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->vals, 0, (cap * kSymBlock + vpad) * 4);
   if (e == cudaSuccess) e = cudaMemset(h->colind, 0, (cap + vpad) * 4);
   if (e == cudaSuccess) e = cudaMemset(h->rowptr, 0, (n + 1 + vpad) * 4);
   for (float* v : {h->dv, h->rhs})
@@ -412,11 +412,13 @@ int pcloth_export(pcloth_t ht, int32_t* rowptr, int32_t* colind, float* vals,
   if (rowptr) e = cudaMemcpyAsync(rowptr, h->rowptr, (n + 1) * 4, cudaMemcpyDefault, h->stream);
   if (colind && e == cudaSuccess)
     e = cudaMemcpyAsync(colind, h->colind, size_t(nnzb) * 4, cudaMemcpyDefault, h->stream);
-  if (vals && e == cudaSuccess)
-    e = cudaMemcpyAsync(vals, h->vals, size_t(nnzb) * 36, cudaMemcpyDefault, h->stream);
   if (b && e == cudaSuccess)
     e = cudaMemcpyAsync(b, h->rhs, n * 12, cudaMemcpyDefault, h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "export copy");
+  if (vals) {
+    rc = launch_vals_expand(h, vals, nnzb);   // packed symmetric -> row-major 3x3
+    if (rc != PCLOTH_OK) return rc;
+  }
   if (pinv) {
     rc = launch_pinv_expand(h, pinv);
     if (rc != PCLOTH_OK) return rc;

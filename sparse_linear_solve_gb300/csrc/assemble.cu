@@ -21,7 +21,10 @@
 // No float atomics: every sum has a fixed order, so the assembled system is
 // bitwise reproducible.  Each off-diagonal block is computed by its own row;
 // the block (j, i) is computed from the negated edge vector and is therefore
-// bitwise equal to the block (i, j).
+// bitwise equal to the block (i, j).  Every block is a symmetric 3x3 (a sum
+// of element stiffnesses k[a I + c d d^T], plus m I on the diagonal) and is
+// stored packed, six floats (a00 a01 a02 a11 a12 a22) per block, which cuts
+// the bytes every SpMV streams by a third.
 
 #include "pcloth_internal.cuh"
 
@@ -257,7 +260,8 @@ struct RowInfo {
 };
 
 // Computes block `o` (absolute output index) of tile-local row `ri`; writes
-// the value (9 floats, -h^2 sum K) and the force sum into shared staging.
+// the value (-h^2 sum K as a packed symmetric block, 6 floats) and the force
+// sum into shared staging.
 __device__ __forceinline__ void compute_block(const AsmArgs& a, int32_t i, const RowInfo& R,
                                               int32_t p, float* __restrict__ stv,
                                               float* __restrict__ stf, int32_t* __restrict__ stc,
@@ -308,9 +312,8 @@ __device__ __forceinline__ void compute_block(const AsmArgs& a, int32_t i, const
       }
     }
   }
-  stv[0] = K[0]; stv[1] = K[1]; stv[2] = K[2];
-  stv[3] = K[1]; stv[4] = K[3]; stv[5] = K[4];
-  stv[6] = K[2]; stv[7] = K[4]; stv[8] = K[5];
+#pragma unroll
+  for (int t = 0; t < kSymBlock; ++t) stv[t] = K[t];
   stf[0] = F[0]; stf[1] = F[1]; stf[2] = F[2];
   *stc = col;
 }
@@ -324,11 +327,11 @@ __device__ __forceinline__ void compute_block(const AsmArgs& a, int32_t i, const
 // ~0.1%, which the soft modes of the system amplify.
 __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const float (&Ks)[6],
                                            const float (&Kc)[6], const float (&Fs)[3],
-                                           float* __restrict__ D) {
+                                           float (&D)[kSymBlock]) {
   const float m = a.mass[i];
+  // packed symmetric diagonal block (d00 d01 d02 d11 d12 d22)
   D[0] = Ks[0] + (Kc[0] + m); D[1] = Ks[1] + Kc[1]; D[2] = Ks[2] + Kc[2];
-  D[3] = D[1]; D[4] = Ks[3] + (Kc[3] + m); D[5] = Ks[4] + Kc[4];
-  D[6] = D[2]; D[7] = D[5]; D[8] = Ks[5] + (Kc[5] + m);
+  D[3] = Ks[3] + (Kc[3] + m); D[4] = Ks[4] + Kc[4]; D[5] = Ks[5] + (Kc[5] + m);
   const float b0 = a.dt * (Fs[0] + m * a.gx);
   const float b1 = a.dt * (Fs[1] + m * a.gy);
   const float b2 = a.dt * (Fs[2] + m * a.gz);
@@ -336,27 +339,28 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const fl
   a.rhs[3 * int64_t(i) + 1] = b1;
   a.rhs[3 * int64_t(i) + 2] = b2;
   // inverse of the symmetric block by its adjugate
-  const float c00 = D[4] * D[8] - D[5] * D[7];
-  const float c01 = D[5] * D[6] - D[3] * D[8];
-  const float c02 = D[3] * D[7] - D[4] * D[6];
-  const float c11 = D[0] * D[8] - D[2] * D[6];
-  const float c12 = D[2] * D[3] - D[0] * D[5];
-  const float c22 = D[0] * D[4] - D[1] * D[3];
-  const float det = D[0] * c00 + D[1] * c01 + D[2] * c02;
+  const float d00 = D[0], d01 = D[1], d02 = D[2], d11 = D[3], d12 = D[4], d22 = D[5];
+  const float c00 = d11 * d22 - d12 * d12;
+  const float c01 = d12 * d02 - d01 * d22;
+  const float c02 = d01 * d12 - d11 * d02;
+  const float c11 = d00 * d22 - d02 * d02;
+  const float c12 = d02 * d01 - d00 * d12;
+  const float c22 = d00 * d11 - d01 * d01;
+  const float det = d00 * c00 + d01 * c01 + d02 * c02;
   const float id = 1.0f / det;
   // the inverse of a symmetric block is symmetric: six entries, two float4
   a.pinv8[2 * int64_t(i)] = make_float4(c00 * id, c01 * id, c02 * id, c11 * id);
   a.pinv8[2 * int64_t(i) + 1] = make_float4(c12 * id, c22 * id, 0.f, 0.f);
   bool ok = finite3(b0, b1, b2) && isfinite(det) && det > 0.0f;
 #pragma unroll
-  for (int t = 0; t < 9; ++t) ok = ok && isfinite(D[t]);
+  for (int t = 0; t < kSymBlock; ++t) ok = ok && isfinite(D[t]);
   if (!ok) atomicOr(a.status, ST_NONFINITE);
 }
 
 __global__ void __launch_bounds__(kAsmThreads)
 assemble_rows(AsmArgs a) {
   __shared__ RowInfo rows[kAsmRows + 1];
-  __shared__ float stv[kAsmCap * 9];
+  __shared__ float stv[kAsmCap * kSymBlock];
   __shared__ float stf[kAsmCap * 3];
   __shared__ int32_t stc[kAsmCap];
   __shared__ double red[9][kAsmThreads / 32];
@@ -412,7 +416,8 @@ assemble_rows(AsmArgs a) {
           if (rows[mid].ob <= gob + o) lo = mid; else hi = mid - 1;
         }
         const RowInfo R = rows[lo];
-        compute_block(a, r0 + lo, R, gob + o - R.ob, &stv[9 * o], &stf[3 * o], &stc[o], m_valid);
+        compute_block(a, r0 + lo, R, gob + o - R.ob, &stv[kSymBlock * o], &stf[3 * o], &stc[o],
+                      m_valid);
       }
       __syncthreads();
       // phase 3: one thread per row reduces its blocks into the diagonal
@@ -425,11 +430,10 @@ assemble_rows(AsmArgs a) {
         int32_t dpos = -1;
         for (int32_t o = o0; o < o1; ++o) {
           if (stc[o] == i) { dpos = o; continue; }
-          const float* s = &stv[9 * o];
-          const float v6[6] = {s[0], s[1], s[2], s[4], s[5], s[8]};
+          const float* s = &stv[kSymBlock * o];
 #pragma unroll
           for (int t = 0; t < 6; ++t) {
-            const float x = -v6[t];
+            const float x = -s[t];
             const float sum = Ks[t] + x;
             const float bp = sum - Ks[t];
             Kc[t] += (Ks[t] - (sum - bp)) + (x - bp);
@@ -437,19 +441,19 @@ assemble_rows(AsmArgs a) {
           }
           Fs[0] += stf[3 * o]; Fs[1] += stf[3 * o + 1]; Fs[2] += stf[3 * o + 2];
         }
-        float D[9];
+        float D[kSymBlock];
         finish_row(a, i, Ks, Kc, Fs, D);
         if (dpos >= 0) {
 #pragma unroll
-          for (int t = 0; t < 9; ++t) stv[9 * dpos + t] = D[t];
+          for (int t = 0; t < kSymBlock; ++t) stv[kSymBlock * dpos + t] = D[t];
         } else {
           atomicOr(a.status, ST_CAPACITY);  // diagonal missing: cannot happen
         }
       }
       __syncthreads();
       // phase 4: coalesced write-out of values and column indices
-      float* dst = a.vals + 9 * int64_t(gob);
-      for (int32_t f = threadIdx.x; f < 9 * nblk; f += kAsmThreads) dst[f] = stv[f];
+      float* dst = a.vals + kSymBlock * int64_t(gob);
+      for (int32_t f = threadIdx.x; f < kSymBlock * nblk; f += kAsmThreads) dst[f] = stv[f];
       for (int32_t o = threadIdx.x; o < nblk; o += kAsmThreads) a.colind[gob + o] = stc[o];
       __syncthreads();
     } else {
@@ -462,16 +466,16 @@ assemble_rows(AsmArgs a) {
         const int32_t cn = min(kAsmCap, nblk - c0);
         __syncthreads();
         for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads)
-          compute_block(a, i, R, c0 + o, &stv[9 * o], &stf[3 * o], &stc[o], m_valid);
+          compute_block(a, i, R, c0 + o, &stv[kSymBlock * o], &stf[3 * o], &stc[o], m_valid);
         __syncthreads();
         // fixed-order fp64 partial sums (one row: the cost is negligible):
         // thread t owns blocks t, t+T, ...
         double part[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
         for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads) {
           if (stc[o] == i) { dpos_abs = gob + c0 + o; continue; }
-          const float* s = &stv[9 * o];
+          const float* s = &stv[kSymBlock * o];
           part[0] -= s[0]; part[1] -= s[1]; part[2] -= s[2];
-          part[3] -= s[4]; part[4] -= s[5]; part[5] -= s[8];
+          part[3] -= s[3]; part[4] -= s[4]; part[5] -= s[5];
           part[6] += stf[3 * o]; part[7] += stf[3 * o + 1]; part[8] += stf[3 * o + 2];
         }
 #pragma unroll
@@ -487,8 +491,8 @@ assemble_rows(AsmArgs a) {
           for (int w = 0; w < kAsmThreads / 32; ++w) s += red[threadIdx.x][w];
           acc[threadIdx.x] += s;
         }
-        float* dst = a.vals + 9 * (int64_t(gob) + c0);
-        for (int32_t f = threadIdx.x; f < 9 * cn; f += kAsmThreads) dst[f] = stv[f];
+        float* dst = a.vals + kSymBlock * (int64_t(gob) + c0);
+        for (int32_t f = threadIdx.x; f < kSymBlock * cn; f += kAsmThreads) dst[f] = stv[f];
         for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads) a.colind[gob + c0 + o] = stc[o];
       }
       __syncthreads();
@@ -501,11 +505,11 @@ assemble_rows(AsmArgs a) {
           Kc[t] = float(acc[t] - double(Ks[t]));
         }
         const float Fs[3] = {float(acc[6]), float(acc[7]), float(acc[8])};
-        float D[9];
+        float D[kSymBlock];
         finish_row(a, i, Ks, Kc, Fs, D);
-        float* dst = a.vals + 9 * int64_t(dpos_abs);
+        float* dst = a.vals + kSymBlock * int64_t(dpos_abs);
 #pragma unroll
-        for (int t = 0; t < 9; ++t) dst[t] = D[t];
+        for (int t = 0; t < kSymBlock; ++t) dst[t] = D[t];
       }
       __syncthreads();
     }
@@ -523,7 +527,26 @@ __global__ void pinv_expand(int32_t n, const float4* __restrict__ p8, float* __r
   o[6] = u.z; o[7] = w.x; o[8] = w.y;
 }
 
+// Packed symmetric blocks (a00 a01 a02 a11 a12 a22) to row-major 3x3.
+__global__ void vals_expand(int64_t nnzb, const float* __restrict__ v6, float* __restrict__ out) {
+  const int64_t b = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (b >= nnzb) return;
+  const float* s = v6 + kSymBlock * b;
+  const float a00 = s[0], a01 = s[1], a02 = s[2], a11 = s[3], a12 = s[4], a22 = s[5];
+  float* o = out + 9 * b;
+  o[0] = a00; o[1] = a01; o[2] = a02;
+  o[3] = a01; o[4] = a11; o[5] = a12;
+  o[6] = a02; o[7] = a12; o[8] = a22;
+}
+
 }  // namespace
+
+int launch_vals_expand(Handle* h, float* out9, int64_t nnzb) {
+  if (nnzb <= 0) return PCLOTH_OK;
+  vals_expand<<<unsigned((nnzb + 255) / 256), 256, 0, h->stream>>>(nnzb, h->vals, out9);
+  h->launches += 1;
+  return check_launch(h, "vals expand");
+}
 
 int launch_pinv_expand(Handle* h, float* out9) {
   pinv_expand<<<(h->n + 255) / 256, 256, 0, h->stream>>>(h->n, h->pinv8, out9);

@@ -439,6 +439,7 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
   h.rowptr = const_cast<int32_t*>(rowptr);
   h.colind = const_cast<int32_t*>(colind);
   h.vals = const_cast<float*>(vals);
+  h.blk = 9;   // the caller's blocks are general row-major 3x3
   h.rhs = const_cast<float*>(b);
 
   const int vg = h.vec_grid;

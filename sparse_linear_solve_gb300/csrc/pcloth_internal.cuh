@@ -44,6 +44,7 @@ constexpr int kScanThreads = 256;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;
 
+constexpr int kSymBlock = 6;   // floats per packed symmetric 3x3 block
 constexpr int kAsmRows = 32;      // rows per assembly tile
 constexpr int kAsmCap = 768;      // blocks staged per assembly group
 constexpr int kAsmThreads = 256;
@@ -89,7 +90,12 @@ struct Handle {
   // assembled system
   int32_t* rowptr = nullptr;     // n+1
   int32_t* colind = nullptr;     // nnzb_cap (+pad)
-  float* vals = nullptr;         // nnzb_cap*9 (+pad)
+  // Block values.  Every block of A is a symmetric 3x3 (a sum of symmetric
+  // element stiffnesses, plus m I on the diagonal), so the library stores
+  // six floats per block, (a00 a01 a02 a11 a12 a22): 24 bytes instead of 36.
+  // A caller's general BSR3 (allocation-free solve) has blk = 9, row-major.
+  float* vals = nullptr;         // nnzb_cap*blk (+pad)
+  int32_t blk = kSymBlock;       // floats per block in vals
   float* rhs = nullptr;          // 3n
   float4* pinv8 = nullptr;       // 2 per vertex: (P00 P01 P02 P11) (P12 P22 0 0)
 
@@ -168,6 +174,8 @@ int launch_spmv_pcg(Handle* h, int k, double tol);  // k = 0-based iteration
 
 // assemble.cu: expand the packed symmetric inverses to float[n][3][3]
 int launch_pinv_expand(Handle* h, float* out9);
+// assemble.cu: expand the packed symmetric blocks to float[nnzb][3][3]
+int launch_vals_expand(Handle* h, float* out9, int64_t nnzb);
 
 // pcg.cu
 int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv,

@@ -63,14 +63,21 @@ constexpr int kPipeConsumers = 32 * kPipeConsumerWarps;
 constexpr int kPipeThreads = 32 + kPipeConsumers;
 constexpr int kPipePerThread = (kPipeCap + kPipeConsumers - 1) / kPipeConsumers;
 constexpr int kPipeRpInts = kPipeRows + 4;
-constexpr int kPipeValBytes = kPipeCap * 36 + 32;
 constexpr int kPipeColBytes = kPipeCap * 4 + 32;
-constexpr int kPipeStageBytes =
-    ((kPipeRpInts * 4 + kPipeValBytes + kPipeColBytes) + 127) / 128 * 128;
 constexpr int kPipeHeadBytes = 256;           // barriers and descriptors
 constexpr int kPipePartBytes = kPipeCap * 16; // one float4 of products per block
-constexpr size_t kPipeSmem = size_t(kPipeHeadBytes) + size_t(kPipeStages) * kPipeStageBytes +
-                             2 * size_t(kPipePartBytes);
+
+// Shared-memory geometry of one stage for blocks of BW floats: row pointers,
+// block values, column indices (each copy window has 16-byte slack at both
+// ends), then the double-buffered products after the stages.
+template <int BW>
+struct Pipe {
+  static constexpr int kValBytes = kPipeCap * 4 * BW + 32;
+  static constexpr int kStageBytes =
+      ((kPipeRpInts * 4 + kValBytes + kPipeColBytes) + 127) / 128 * 128;
+  static constexpr size_t kSmem = size_t(kPipeHeadBytes) + size_t(kPipeStages) * kStageBytes +
+                                  2 * size_t(kPipePartBytes);
+};
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legal wait
 static_assert(kPipeRows % 4 == 0, "row-pointer copies must start 16-byte aligned");
 static_assert(kPipeRows <= kPipeConsumers, "one consumer per row");
@@ -192,9 +199,30 @@ __device__ __forceinline__ float3 gather_x(const SpmvArgs& a, int32_t col, float
   return make_float3(a.in[c3], a.in[c3 + 1], a.in[c3 + 2]);
 }
 
-template <bool PCG>
+// Product of one block with x.  BW = 6: packed symmetric block
+// (a00 a01 a02 a11 a12 a22), read as three 8-byte words (a thread's stride of
+// 24 bytes keeps the 16 threads of each half-warp on distinct banks); BW = 9:
+// general row-major block.  Both give the same bits for a symmetric block.
+template <int BW>
+__device__ __forceinline__ float4 block_times(const float* __restrict__ B, float3 x) {
+  if (BW == kSymBlock) {
+    const float2* B2 = reinterpret_cast<const float2*>(B);
+    const float2 u = B2[0], v = B2[1], w = B2[2];   // (a00 a01) (a02 a11) (a12 a22)
+    return make_float4(fmaf(u.x, x.x, fmaf(u.y, x.y, v.x * x.z)),
+                       fmaf(u.y, x.x, fmaf(v.y, x.y, w.x * x.z)),
+                       fmaf(v.x, x.x, fmaf(w.x, x.y, w.y * x.z)), 0.f);
+  }
+  return make_float4(fmaf(B[0], x.x, fmaf(B[1], x.y, B[2] * x.z)),
+                     fmaf(B[3], x.x, fmaf(B[4], x.y, B[5] * x.z)),
+                     fmaf(B[6], x.x, fmaf(B[7], x.y, B[8] * x.z)), 0.f);
+}
+
+template <bool PCG, int BW>
 __global__ void __launch_bounds__(kPipeThreads)
 spmv_pipe(SpmvArgs a) {
+  static_assert(BW == kSymBlock || BW == 9, "block width");
+  constexpr int kPipeStageBytes = Pipe<BW>::kStageBytes;
+  constexpr int kPipeValBytes = Pipe<BW>::kValBytes;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kPipeStages;
@@ -232,15 +260,15 @@ spmv_pipe(SpmvArgs a) {
           const int32_t c1 = min(b1, c0 + kPipeCap);
           if (!wait_bounded(&empty[s], ph ^ 1u)) { ok = false; break; }
           unsigned char* st = stages + size_t(s) * kPipeStageBytes;
-          const int64_t va0 = (int64_t(c0) * 36) & ~int64_t(15);
-          const int64_t va1 = (int64_t(c1) * 36 + 15) & ~int64_t(15);
+          const int64_t va0 = (int64_t(c0) * (4 * BW)) & ~int64_t(15);
+          const int64_t va1 = (int64_t(c1) * (4 * BW) + 15) & ~int64_t(15);
           const int64_t ca0 = (int64_t(c0) * 4) & ~int64_t(15);
           const int64_t ca1 = (int64_t(c1) * 4 + 15) & ~int64_t(15);
           const uint32_t rp_bytes = uint32_t(((nrows + 1 + 3) & ~3) * 4);
           const uint32_t v_bytes = uint32_t(va1 - va0), c_bytes = uint32_t(ca1 - ca0);
           StageDesc d;
           d.tile = tile; d.r0 = r0; d.nrows = nrows; d.c0 = c0; d.c1 = c1;
-          d.voff = int32_t((int64_t(c0) * 36 - va0) >> 2);
+          d.voff = int32_t((int64_t(c0) * (4 * BW) - va0) >> 2);
           d.coff = int32_t((int64_t(c0) * 4 - ca0) >> 2);
           d.flags = (c0 == b0 ? 1 : 0) | (c1 == b1 ? 2 : 0);
           desc[s] = d;
@@ -306,13 +334,7 @@ spmv_pipe(SpmvArgs a) {
 #pragma unroll
         for (int u = 0; u < kPipePerThread; ++u) {
           const int j = ct + u * kPipeConsumers;
-          if (col[u] >= 0) {
-            const float* B = sv + 9 * j;
-            const float3 x = xv[u];
-            part[j] = make_float4(fmaf(B[0], x.x, fmaf(B[1], x.y, B[2] * x.z)),
-                                  fmaf(B[3], x.x, fmaf(B[4], x.y, B[5] * x.z)),
-                                  fmaf(B[6], x.x, fmaf(B[7], x.y, B[8] * x.z)), 0.f);
-          }
+          if (col[u] >= 0) part[j] = block_times<BW>(sv + BW * j, xv[u]);
         }
       }
       named_barrier_sync(1, kPipeConsumers);
@@ -360,26 +382,28 @@ bool g_attr_done[64] = {};
 
 // Shared-memory carveout: just enough for kPipeCtasPerSm CTAs, so that the
 // rest of the unified L1/shared storage stays L1 cache for the gathers.
-int carveout_percent() {
-  const size_t need = size_t(kPipeCtasPerSm) * (kPipeSmem + 2048);
+int carveout_percent(size_t smem) {
+  const size_t need = size_t(kPipeCtasPerSm) * (smem + 2048);
   const size_t max_smem = 228 * 1024;
   int pct = int((need * 100 + max_smem - 1) / max_smem);
   return pct > 100 ? 100 : pct;
 }
 
+template <typename F>
+cudaError_t set_attrs(F* f, size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(smem));
+  if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
+    e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             carveout_percent(smem));
+  return e;
+}
+
 int ensure_attr(Handle* h) {
   if (h->device >= 0 && h->device < 64 && g_attr_done[h->device]) return PCLOTH_OK;
-  cudaError_t e = cudaFuncSetAttribute(spmv_pipe<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(kPipeSmem));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(spmv_pipe<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kPipeSmem));
-  if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
-    e = cudaFuncSetAttribute(spmv_pipe<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             carveout_percent());
-  if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
-    e = cudaFuncSetAttribute(spmv_pipe<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             carveout_percent());
+  cudaError_t e = set_attrs(spmv_pipe<false, kSymBlock>, Pipe<kSymBlock>::kSmem);
+  if (e == cudaSuccess) e = set_attrs(spmv_pipe<true, kSymBlock>, Pipe<kSymBlock>::kSmem);
+  if (e == cudaSuccess) e = set_attrs(spmv_pipe<true, 9>, Pipe<9>::kSmem);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(spmv)");
   if (h->device >= 0 && h->device < 64) g_attr_done[h->device] = true;
   return PCLOTH_OK;
@@ -409,7 +433,9 @@ int launch_spmv(Handle* h, const float* in, float* out) {
   SpmvArgs a = base_args(h);
   a.in = in;
   a.out = out;
-  spmv_pipe<false><<<h->spmv_grid, kPipeThreads, kPipeSmem, h->stream>>>(a);
+  if (h->blk != kSymBlock) return fail(h, PCLOTH_ERR_INVALID_ARG, "spmv: packed blocks only");
+  spmv_pipe<false, kSymBlock>
+      <<<h->spmv_grid, kPipeThreads, Pipe<kSymBlock>::kSmem, h->stream>>>(a);
   h->launches += 1;
   return check_launch(h, "spmv");
 }
@@ -432,7 +458,11 @@ int launch_spmv_pcg(Handle* h, int k, double tol) {
   a.first = (k == 0);
   a.k = k;
   a.tol2 = tol * tol;
-  spmv_pipe<true><<<h->spmv_grid, kPipeThreads, kPipeSmem, h->stream>>>(a);
+  if (h->blk == kSymBlock)
+    spmv_pipe<true, kSymBlock>
+        <<<h->spmv_grid, kPipeThreads, Pipe<kSymBlock>::kSmem, h->stream>>>(a);
+  else
+    spmv_pipe<true, 9><<<h->spmv_grid, kPipeThreads, Pipe<9>::kSmem, h->stream>>>(a);
   h->launches += 1;
   return check_launch(h, "spmv (pcg)");
 }
