@@ -66,23 +66,28 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+TRAFFIC_FILE = "pcg_loop_folded_stack_C5_traffic.json"
+KERNEL_SOURCES = ("spmv_pipe.cuh", "pcg.cu", "async_copy.cuh", "pcloth_internal.cuh")
+
+
 def stored_traffic(kernel_src_digest):
-    """DRAM bytes per launch of the PCG SpMV from the committed ncu summary,
-    only if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "spmv_pipe_pcg_folded_stack_C5_traffic.json")
+    """DRAM bytes per PCG iteration of the persistent PCG kernel from the
+    committed ncu summary, only if it was taken on the current kernel
+    source."""
+    path = os.path.join(ROOT, "profiles", TRAFFIC_FILE)
     try:
         with open(path) as f:
             d = json.load(f)
         if d.get("source_digest") == kernel_src_digest:
-            return float(d["dram_bytes_per_launch"])
+            return float(d["dram_bytes_per_iteration"])
     except Exception:
         pass
     return None
 
 
-def spmv_source_digest():
+def kernel_source_digest():
     h = hashlib.sha256()
-    for f in ("spmv.cu", "pcloth_internal.cuh"):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "sparse_linear_solve_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -238,21 +243,34 @@ def run_ours(args, rank, world, local_rank):
     ms, its, codes, prof_clean = timed_steps(0)
     clk = clocks.stop()
     ms = max_over_ranks(ms, dev)
-    # pass 2: the same K steps again, every kernel launch bracketed by CUDA
-    # events on the library's stream, for the per-kernel averages
+    # pass 2: the same K steps again with CUDA events around every assembly
+    # and every PCG launch on the library's stream, and the PCG kernel's own
+    # phase timers
     ms_prof, its_prof, _, prof = timed_steps(2)
     nnzb_seen = [cloth.nnzb()]
 
-    # ---- roofline of the dominant kernel: the PCG SpMV -------------------
+    # ---- roofline of the dominant kernel: the persistent PCG -------------
+    # Algorithmic bytes per PCG iteration: the matrix once (28 B/block:
+    # 24 packed symmetric values + 4 colind; 4 B/row rowptr), p read once and
+    # q written (24 B/row), the update phase (dv, p, q, r read, the
+    # symmetric P read 24 B, dv, r, z written: 108 B/row) and the
+    # direction update (z, p read, p written: 36 B/row).  Per launch: that
+    # times the iterations, plus the start (b 12, P 24 read; r, z, p, dv
+    # written 48) and dv out (12 + 12) = 108 B/row.
     n = w.n_verts
     nnzb = nnzb_seen[-1]
-    bytes_per_launch = 28 * nnzb + 52 * n
+    it_bytes = 28 * nnzb + 172 * n
+    spmv_bytes = 28 * nnzb + 28 * n
+    vec_bytes = 144 * n
+    iters = max(prof["iterations"], 1)
+    solves = max(prof["solves"], 1)
+    launch_bytes = (iters * it_bytes + solves * 108 * n) / solves
+    launch_ms = prof["solve_ms"] / solves
+    achieved = launch_bytes / (launch_ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
     samples = max(prof["samples"], 1)
     spmv_avg_ms = prof["spmv_ms"] / samples
-    achieved = bytes_per_launch / (spmv_avg_ms * 1e-3) / 1e9
-    peak, peak_src = hbm_peak()
-    upd_bytes = 120 * n  # dv, p, r, q, P(36) read; dv, r, z written (bytes/vertex)
-    upd_avg_ms = prof["update_ms"] / samples
+    vec_avg_ms = prof["update_ms"] / samples
 
     # ---- end to end through the host-buffer entry point ------------------
     e2e = None
@@ -298,20 +316,26 @@ def run_ours(args, rank, world, local_rank):
         pcg_iterations_per_s_solve_only=sum(its_prof) / (prof["solve_ms"] * 1e-3),
         pcg_iterations_mean=sum(its) / K,
         assembly_ms=prof["assemble_ms"] / max(prof["assemble_calls"], 1),
-        spmv_gbs=achieved,
-        spmv_us=spmv_avg_ms * 1e3,
-        update_us=upd_avg_ms * 1e3,
-        update_gbs=upd_bytes / (upd_avg_ms * 1e-3) / 1e9 if upd_avg_ms > 0 else None,
+        spmv_phase_us=spmv_avg_ms * 1e3,
+        spmv_phase_gbs=spmv_bytes / (spmv_avg_ms * 1e-3) / 1e9 if spmv_avg_ms > 0 else None,
+        vector_phases_us=vec_avg_ms * 1e3,
+        vector_phases_gbs=vec_bytes / (vec_avg_ms * 1e-3) / 1e9 if vec_avg_ms > 0 else None,
+        iteration_us=launch_ms * 1e3 / (iters / solves),
         codes=sorted(set(codes)),
-        roofline=dict(bound="hbm", kernel="spmv_pipe<true> (PCG SpMV, fused p update + p.q)",
-                      timing="CUDA events on the library stream around every SpMV launch of a "
-                             "second pass over the same %d steps (%d launches, %.1f ms/step "
-                             "with the events)" % (K, prof["samples"], ms_prof / K),
+        roofline=dict(bound="hbm", kernel="pcg_loop<6> (persistent PCG: streaming SpMV, "
+                                          "update and direction phases, grid barriers)",
+                      timing="CUDA events on the library stream around each PCG launch (one "
+                             "per solve) of a second pass over the same %d steps (%d launches, "
+                             "%.1f ms/step with the events)" % (K, prof["solves"], ms_prof / K),
                       achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
-                      peak_source=peak_src, bytes_per_launch=bytes_per_launch,
-                      bytes_model="28 B/block (24 packed symmetric values + 4 colind) + 52 B/row (rowptr 4, "
-                                  "z 12, p_old 12 read; p 12, q 12 written)",
-                      traffic=stored_traffic(spmv_source_digest())),
+                      peak_source=peak_src, bytes_per_launch=launch_bytes,
+                      bytes_model="per iteration 28 B/block (24 packed symmetric values + "
+                                  "4 colind) + 172 B/row (rowptr 4; SpMV p 12 read, q 12 "
+                                  "written; update dv p q r 48 + P 24 read, dv r z 36 "
+                                  "written; direction z p 24 read, p 12 written); per launch "
+                                  "+108 B/row (start and dv out)",
+                      traffic=(None if stored_traffic(kernel_source_digest()) is None else
+                               stored_traffic(kernel_source_digest()) * iters / solves)),
         clocks=clk,
         gpu_launches=int(prof_clean["kernel_launches"]),
         e2e=e2e,

@@ -95,13 +95,11 @@ typedef struct {
 
 /* Options: max_contacts sizes the per-step contact buffers; device is the
  * CUDA device ordinal; stream is a cudaStream_t (0 = the legacy default
- * stream).  max_iter_chunk: PCG iterations enqueued between convergence
- * polls (0 = default 16). */
+ * stream). */
 typedef struct {
   int32_t max_contacts;
   int device;
   void* stream;
-  int32_t max_iter_chunk;
 } pcloth_opts;
 
 /* Create a handle for a cloth and its (static) springs.  Copies the springs
@@ -129,8 +127,10 @@ int pcloth_spmv(pcloth_t h, const float* in, float* out);
 /* Solve A dv = b by block-Jacobi PCG from dv = 0 until
  * |r|_2 <= tol |b|_2 (recursive residual) or maxit iterations; dv is device
  * float32[n][3]; *iterations and *rel_residual (= |r|/|b|) are written on
- * the host.  Sec. 3.1 / Eq. (3).  Synchronises at the end (and polls the
- * device every max_iter_chunk iterations without stalling it). */
+ * the host.  Sec. 3.1 / Eq. (3).  The whole solve is one cooperative kernel
+ * launch (all of its CTAs resident; grid-wide barriers between the SpMV and
+ * vector phases of each iteration), so the host does not take part in the
+ * iteration.  Synchronises at the end. */
 int pcloth_solve(pcloth_t h, double tol, int32_t maxit, float* dv,
                  int32_t* iterations, double* rel_residual);
 
@@ -171,17 +171,16 @@ int pcloth_sync(pcloth_t h);
  * the message of the last failed pcloth_create. */
 const char* pcloth_last_error(pcloth_t h);
 
-/* Profiling: while enabled, the library records CUDA events on its stream
- * around every assembly and solve, and around the two launches (SpMV, PCG
- * update) of the first iteration of every polling chunk (on = 1) or of every
- * iteration (on = 2), and accumulates their device time; on = 0 disables.
- * Iterations launched after convergence (they return at once) are not
- * sampled.  pcloth_profile_read fills ms_out[4] = {assembly, sampled PCG
- * SpMV, sampled PCG update, whole solves} in milliseconds and counts_out[7] =
- * {assemblies, SpMV launches, update launches, solves, PCG iterations,
- * kernels launched by this handle, sampled iterations}; divide the sampled
- * times by the sample count for a per-launch average.  reset != 0 zeroes the
- * accumulators and keeps the profiling mode. */
+/* Profiling: while enabled (on != 0; 1 and 2 behave alike), the library
+ * records CUDA events on its stream around every assembly and around every
+ * launch of the PCG kernel, and the PCG kernel times its phases with the
+ * GPU's global timer (the SpMV phase up to the barrier after it; the two
+ * vector phases up to theirs).  pcloth_profile_read fills ms_out[4] =
+ * {assembly, PCG SpMV phases, PCG vector phases, PCG kernel launches} in
+ * milliseconds and counts_out[7] = {assemblies, SpMV phases, vector-phase
+ * pairs, solves, PCG iterations, kernels launched by this handle, timed SpMV
+ * phases}; divide a phase time by the timed count for a per-iteration
+ * average.  reset != 0 zeroes the accumulators and keeps the mode. */
 int pcloth_profile_enable(pcloth_t h, int on);
 int pcloth_profile_read(pcloth_t h, double* ms_out, int64_t* counts_out,
                         int reset);

@@ -38,18 +38,14 @@ void free_handle(Handle* h) {
                   h->sort_counts, h->flags, h->scan_tmp, h->newkey,
                   h->newfirst, h->tile_nb, h->tile_eb, h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
-                  h->dv, h->dv4, h->r4, h->z4, h->p4[0], h->p4[1], h->q4, h->red_spmv,
-                  h->red_upd[0], h->red_upd[1], h->red_init, h->state,
-                  h->d_status};
+                  h->dv, h->dv4, h->r4, h->z4, h->p4, h->q4, h->rec, h->bar,
+                  h->phase_ns, h->state, h->d_status};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (h->state_host) cudaFreeHost(h->state_host);
   if (h->h_status) cudaFreeHost(h->h_status);
+  if (h->phase_host) cudaFreeHost(h->phase_host);
   for (auto& e : h->ev)
-    if (e) cudaEventDestroy(e);
-  for (auto& e : h->pev)
-    if (e) cudaEventDestroy(e);
-  for (auto& e : h->chunk_ev)
     if (e) cudaEventDestroy(e);
   delete h;
 }
@@ -132,7 +128,6 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   h->n = int32_t(n);
   h->ns = int32_t(ns);
   h->max_contacts = int32_t(mc);
-  h->chunk = opts->max_iter_chunk > 0 ? opts->max_iter_chunk : 16;
   for (int c = 0; c < 3; ++c) h->gravity[c] = mesh->gravity[c];
   h->key_bits = bits_for(n);
   h->nnzb_cap = cap;
@@ -209,7 +204,13 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   const int64_t scan_tiles = (ent2 + kScanTile - 1) / kScanTile;
   const int64_t asm_tiles = (n + kAsmRows - 1) / kAsmRows;
   h->spmv_grid = spmv_grid_for(int32_t(n), h->sm_count);
-  const int64_t red_grid = h->spmv_grid;
+  {
+    const int ge = pcg_loop_grid(kSymBlock, int32_t(n), h->device, h->sm_count, &h->loop_grid);
+    if (ge != 0) {
+      free_handle(h);
+      return cuda_fail(nullptr, cudaError_t(ge), "PCG kernel occupancy");
+    }
+  }
   h->vec_grid = int(std::min<int64_t>((n + kVecThreads - 1) / kVecThreads,
                                       int64_t(h->sm_count) * 4));
   const int64_t vpad = 64;  // floats of slack after each vector / value array
@@ -228,8 +229,6 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   for (int b = 0; b < 2; ++b) {
     A(dalloc(&h->ckey[b], ent2));
     A(dalloc(&h->cval[b], ent2));
-    A(dalloc(&h->p4[b], n + vpad));
-    A(dalloc(&h->red_upd[b], int64_t(h->vec_grid) * kRedSlots));
   }
   A(dalloc(&h->sort_counts, sort_tiles * kSortRadix + 1));
   A(dalloc(&h->flags, ent2 + 1));
@@ -250,16 +249,16 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->r4, n + vpad));
   A(dalloc(&h->z4, n + vpad));
   A(dalloc(&h->q4, n + vpad));
-  A(dalloc(&h->red_spmv, red_grid * kRedSlots));
-  A(dalloc(&h->red_init, int64_t(h->vec_grid) * kRedSlots));
+  A(dalloc(&h->p4, n + vpad));
+  A(dalloc(&h->rec, int64_t(h->loop_grid) * kRecSlots));
+  A(dalloc(&h->bar, 1));
+  A(dalloc(&h->phase_ns, 4));
   A(dalloc(&h->state, 1));
   A(dalloc(&h->d_status, 1));
-  A(cudaMallocHost(reinterpret_cast<void**>(&h->state_host), 2 * sizeof(PcgState)));
+  A(cudaMallocHost(reinterpret_cast<void**>(&h->state_host), sizeof(PcgState)));
+  A(cudaMallocHost(reinterpret_cast<void**>(&h->phase_host), 4 * sizeof(unsigned long long)));
   A(cudaMallocHost(reinterpret_cast<void**>(&h->h_status), sizeof(uint32_t)));
   for (auto& ev : h->ev) A(cudaEventCreate(&ev));
-  for (auto& ev : h->chunk_ev) A(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
-  h->pev.assign(size_t(2) * (2 * h->chunk + 1), nullptr);
-  for (auto& ev : h->pev) A(cudaEventCreate(&ev));
   if (!ok) {
     cudaGetLastError();
     free_handle(h);
@@ -279,7 +278,7 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   if (e == cudaSuccess) e = cudaMemset(h->rowptr, 0, (n + 1 + vpad) * 4);
   for (float* v : {h->dv, h->rhs})
     if (e == cudaSuccess) e = cudaMemset(v, 0, (3 * n + vpad) * 4);
-  for (float4* v : {h->dv4, h->r4, h->z4, h->q4, h->p4[0], h->p4[1]})
+  for (float4* v : {h->dv4, h->r4, h->z4, h->q4, h->p4})
     if (e == cudaSuccess) e = cudaMemset(v, 0, (n + vpad) * sizeof(float4));
   if (e == cudaSuccess) e = cudaMemset(h->pinv8, 0, (2 * n + vpad) * sizeof(float4));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 4);

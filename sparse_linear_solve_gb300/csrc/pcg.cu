@@ -4,33 +4,36 @@
 // the inverses of the 3x3 diagonal blocks), plus the backward-Euler state
 // update v += dv, x += h v.
 //
-// One iteration is two kernels:
-//   spmv_tiles<true>  p_k = z_k + beta p_{k-1} (formed where gathered),
-//                     q = A p_k, partial p_k . q
-//   pcg_update        alpha = (r.z)/(p.q); dv += alpha p; r -= alpha q;
-//                     z = P r; partials r.z and r.r
-// Every scalar (alpha, beta, the convergence test |r| <= tol |b|) is formed
-// on the device by each CTA from the previous kernel's per-CTA partials in a
-// fixed order, so no host round trip is needed inside the loop and the
-// iteration is bitwise reproducible.  Dot products accumulate a few terms in
-// fp32 per thread and everything after that in fp64.  The host enqueues
-// `chunk` iterations at a time and reads the device state of the previous
-// chunk while the current one runs; kernels enqueued after convergence
-// return at once.
+// The whole solve is one persistent kernel, launched cooperatively so that
+// all of its CTAs are resident at once.  Each CTA owns the rows of its SpMV
+// tiles (blockIdx.x, +gridDim.x, ...) in every phase, and the phases of an
+// iteration are separated by grid-wide barriers:
+//
+//   S  q = A p (the streaming SpMV of spmv_pipe.cuh, gathering p only);
+//      partial p.q over the CTA's rows                              barrier
+//   U  alpha = r.z / p.q; dv += alpha p; r -= alpha q; z = P r;
+//      partials r.z and r.r                                         barrier
+//   P  stop if |r| <= tol |b| (or breakdown, or maxit); otherwise
+//      beta = r.z / r.z_old and p = z + beta p                      barrier
+//
+// Every scalar is formed by every CTA from the same per-CTA partials in the
+// same order (double-float sums), so all CTAs take the same decisions and
+// the solve is bitwise reproducible.  No host round trip happens inside the
+// solve.  The matrix does not change during a solve, so after deciding to
+// continue, the producer lane already issues the first stages of the next
+// SpMV, and their loads overlap the P phase and the barrier.
+//
+// Every wait (mbarrier, grid barrier) is bounded in time: on a timeout the
+// kernel records ST_WAIT_TIMEOUT, waits (bounded) for its own copies in
+// flight and returns; the host reports an error.
 
 #include <algorithm>
 
-#include "pcloth_internal.cuh"
-
+#include "spmv_pipe.cuh"
 
 namespace pcloth_impl {
 namespace {
 
-// Vector kernels: one thread per vertex on the padded vectors (one float4
-// (x, y, z, 0) per vertex), so every access of a warp is one contiguous,
-// aligned 512-byte transaction; the symmetric block-Jacobi inverse is two
-// float4 per vertex.  Dot products accumulate a vertex's three terms in fp32
-// and everything after that in fp64.
 __device__ __forceinline__ float3 apply_p(float4 u, float4 w, float3 r) {
   // P = [[u.x u.y u.z] [u.y u.w w.x] [u.z w.x w.y]]
   return make_float3(fmaf(u.x, r.x, fmaf(u.y, r.y, u.z * r.z)),
@@ -42,139 +45,329 @@ __device__ __forceinline__ float dot3(float3 a, float3 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, a.z * b.z));
 }
 
-__global__ void __launch_bounds__(kVecThreads)
-pcg_init(int32_t n, const float* __restrict__ b, const float4* __restrict__ pinv8,
-         float4* __restrict__ r, float4* __restrict__ z, float4* __restrict__ dv,
-         float4* __restrict__ p_old, float2* __restrict__ red_rz0,
-         float2* __restrict__ red_bb, PcgState* state) {
-  __shared__ float2 sh[33 * 2];
-  float rz = 0.f, bb = 0.f;
-  for (int64_t i = int64_t(blockIdx.x) * kVecThreads + threadIdx.x; i < n;
-       i += int64_t(gridDim.x) * kVecThreads) {
-    const float3 bv = make_float3(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
-    const float3 zv = apply_p(pinv8[2 * i], pinv8[2 * i + 1], bv);
-    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    r[i] = make_float4(bv.x, bv.y, bv.z, 0.f);
-    z[i] = make_float4(zv.x, zv.y, zv.z, 0.f);
-    dv[i] = zero;
-    p_old[i] = zero;
-    rz += dot3(bv, zv);
-    bb += dot3(bv, bv);
-  }
-  Dfloat v[2] = {df_of(rz), df_of(bb)};
-  block_sum_df<kVecThreads, 2>(v, sh);
-  if (threadIdx.x == 0) {
-    red_rz0[int64_t(blockIdx.x) * kRedSlots + 0] = df_pack(v[0]);
-    red_rz0[int64_t(blockIdx.x) * kRedSlots + 1] = df_pack(v[1]);
-    red_bb[int64_t(blockIdx.x) * kRedSlots + 0] = df_pack(v[1]);
-    if (blockIdx.x == 0) {
-      state->done = 0;
-      state->iterations = 0;
-      state->code = PCLOTH_NOT_CONVERGED;
-      state->relres = 1.0;
-    }
-  }
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// dv += alpha p; r -= alpha q; z = P r; partials of r.z and r.r.  The first
-// vertex's loads are issued before alpha is known, so their latency
-// overlaps the reduction of the previous kernels' partials.
-__global__ void __launch_bounds__(kVecThreads, 4)
-pcg_update(int32_t n, int k, const float4* __restrict__ p, const float4* __restrict__ q,
-           const float4* __restrict__ pinv8, float4* __restrict__ r, float4* __restrict__ z,
-           float4* __restrict__ dv, const float2* __restrict__ red_pq, int npq,
-           const float2* __restrict__ red_rz, const float2* __restrict__ red_bb, int nrz,
-           float2* __restrict__ red_out, PcgState* state, uint32_t* status) {
-  __shared__ float2 sh[33 * 4];
-  __shared__ int flag_sh;
-  __shared__ float alpha_sh;
-  if (threadIdx.x == 0) flag_sh = state->done;
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier.  Every CTA adds 1 to the counter (zeroed before the
+// launch) once per barrier, so the b-th barrier is complete when the counter
+// reaches b * gridDim.x.  The fences make each CTA's writes before the
+// barrier visible to every CTA after it (the release/acquire pattern of a
+// cooperative-groups grid sync).  Returns false, the same in every thread of
+// the CTA, if the wait ran past kWaitNs or any thread of the grid has
+// recorded a timeout: the caller then leaves its loop.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned long long& epoch,
+                                             const uint32_t* status, int* ok_sh) {
   __syncthreads();
-  if (flag_sh) return;
-  const int64_t stride = int64_t(gridDim.x) * kVecThreads;
-  int64_t i = int64_t(blockIdx.x) * kVecThreads + threadIdx.x;
-  float4 pv, qv, rv, dvv, pu, pw;
-  if (i < n) {
-    pv = p[i]; qv = q[i]; rv = r[i]; dvv = dv[i]; pu = pinv8[2 * i]; pw = pinv8[2 * i + 1];
-  }
-  Dfloat v[4];   // p.q, r.z, r.r, b.b
-  v[0] = records_share(red_pq, npq, 0, kVecThreads);
-  v[1] = records_share(red_rz, nrz, 0, kVecThreads);
-  v[2] = records_share(red_rz, nrz, 1, kVecThreads);
-  v[3] = records_share(red_bb, nrz, 0, kVecThreads);
-  block_sum_df<kVecThreads, 4>(v, sh);
   if (threadIdx.x == 0) {
-    const double pq = df_value(v[0]), rz = df_value(v[1]);
-    int stop = 0;
-    if (!(pq > 0.0) || !isfinite(pq) || !isfinite(rz)) {
-      stop = 1;
-      if (blockIdx.x == 0) {
-        const bool fin = isfinite(pq) && isfinite(rz);
-        state->done = 1;
-        state->iterations = k;
-        state->relres = sqrt(df_value(v[2]) / df_value(v[3]));
-        state->code = fin ? PCLOTH_ERR_BREAKDOWN : PCLOTH_ERR_NONFINITE;
-        atomicOr(status, fin ? ST_BREAKDOWN : ST_NONFINITE);
+    ++epoch;
+    const unsigned long long target = epoch * gridDim.x;
+    __threadfence();
+    atomicAdd(bar, 1ull);
+    bool ok = true;
+    if (ld_acquire(bar) < target) {
+      const uint64_t t0 = now_ns();
+      while (ld_acquire(bar) < target) {
+        if (now_ns() - t0 > kWaitNs) {
+          ok = false;
+          break;
+        }
       }
     }
-    alpha_sh = float(rz / pq);
-    flag_sh = stop;
+    __threadfence();
+    *ok_sh = ok && !(ld_acquire(status) & ST_WAIT_TIMEOUT);
   }
   __syncthreads();
-  if (flag_sh) return;
-  const float alpha = alpha_sh;
-  float arz = 0.f, arr = 0.f;
-  while (i < n) {
-    const float3 rn = make_float3(fmaf(-alpha, qv.x, rv.x), fmaf(-alpha, qv.y, rv.y),
-                                  fmaf(-alpha, qv.z, rv.z));
-    const float3 zn = apply_p(pu, pw, rn);
-    dv[i] = make_float4(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
-                        fmaf(alpha, pv.z, dvv.z), 0.f);
-    r[i] = make_float4(rn.x, rn.y, rn.z, 0.f);
-    z[i] = make_float4(zn.x, zn.y, zn.z, 0.f);
-    arz += dot3(rn, zn);
-    arr += dot3(rn, rn);
-    i += stride;
-    if (i < n) {
-      pv = p[i]; qv = q[i]; rv = r[i]; dvv = dv[i]; pu = pinv8[2 * i]; pw = pinv8[2 * i + 1];
+  return *ok_sh != 0;
+}
+
+struct LoopArgs {
+  PipeMatrix m;
+  const float* b;          // float[n][3]
+  const float4* pinv8;     // 2 per vertex
+  float4* dv;
+  float4* r;
+  float4* z;
+  float4* p;
+  float4* q;
+  float2* rec;             // [gridDim.x][kRecSlots]
+  unsigned long long* bar; // grid-barrier counter, zero at launch
+  PcgState* state;
+  uint32_t* status;
+  float* dv_out;           // caller's float[n][3]
+  unsigned long long* phase_ns;  // [4] = S, U, P nanoseconds, timed SpMV phases (or null)
+  double tol2;
+  int32_t maxit;
+};
+
+// The CTA's rows: slot f is row (f % kPipeRows) of its tile number f / kPipeRows.
+__device__ __forceinline__ int32_t own_row(int32_t f) {
+  return (int32_t(blockIdx.x) + (f / kPipeRows) * int32_t(gridDim.x)) * kPipeRows +
+         f % kPipeRows;
+}
+
+struct PGather {
+  const float4* p;
+  __device__ __forceinline__ float3 operator()(int32_t col) const {
+    const float4 v = p[col];
+    return make_float3(v.x, v.y, v.z);
+  }
+};
+
+struct PEpi {
+  const float4* p;
+  float4* q;
+  float pq;
+  __device__ __forceinline__ void operator()(int32_t row, float3 acc) {
+    q[row] = make_float4(acc.x, acc.y, acc.z, 0.f);
+    const float4 pr = p[row];
+    pq = fmaf(pr.x, acc.x, fmaf(pr.y, acc.y, fmaf(pr.z, acc.z, pq)));
+  }
+};
+
+template <int BW>
+__global__ void __launch_bounds__(kPipeThreads, kPipeCtasPerSm)
+pcg_loop(LoopArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const PipeShared sh = pipe_shared<BW>(smem);
+  __shared__ float2 red_sh[33 * 2];
+  __shared__ int ok_sh;
+  __shared__ int stop_sh;
+  __shared__ float scal_sh;
+  pipe_init(sh);
+  __syncthreads();
+
+  const int32_t n = a.m.n;
+  const int32_t tid = threadIdx.x;
+  const int32_t my_tiles = (a.m.ntiles - int32_t(blockIdx.x) + int32_t(gridDim.x) - 1) /
+                           int32_t(gridDim.x);
+  const int32_t nslots = my_tiles * kPipeRows;
+  float2* my_rec = a.rec + size_t(blockIdx.x) * kRecSlots;
+  const bool timer = a.phase_ns != nullptr && blockIdx.x == 0 && tid == 0;
+  unsigned long long epoch = 0;
+  unsigned long long t_s = 0, t_u = 0, t_p = 0, n_timed = 0;
+  Producer P;
+  Consumer C;
+  producer_begin(P);
+  consumer_begin(C);
+
+  // ---- init: r = b, z = P b, dv = 0, p = z; partials r.z and b.b ---------
+  {
+    float rz = 0.f, bb = 0.f;
+    for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+      const int32_t i = own_row(f);
+      if (i >= n) continue;
+      const float3 bv = make_float3(a.b[3 * int64_t(i)], a.b[3 * int64_t(i) + 1],
+                                    a.b[3 * int64_t(i) + 2]);
+      const float3 zv = apply_p(a.pinv8[2 * int64_t(i)], a.pinv8[2 * int64_t(i) + 1], bv);
+      const float4 z4 = make_float4(zv.x, zv.y, zv.z, 0.f);
+      a.r[i] = make_float4(bv.x, bv.y, bv.z, 0.f);
+      a.z[i] = z4;
+      a.p[i] = z4;
+      a.dv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      rz += dot3(bv, zv);
+      bb += dot3(bv, bv);
+    }
+    Dfloat v[2] = {df_of(rz), df_of(bb)};
+    block_sum_df<kPipeThreads, 2>(v, red_sh);
+    if (tid == 0) {
+      my_rec[REC_RZ] = df_pack(v[0]);
+      my_rec[REC_BB] = df_pack(v[1]);
     }
   }
-  Dfloat o[2] = {df_of(arz), df_of(arr)};
-  block_sum_df<kVecThreads, 2>(o, sh);
-  if (threadIdx.x == 0) {
-    red_out[int64_t(blockIdx.x) * kRedSlots + 0] = df_pack(o[0]);
-    red_out[int64_t(blockIdx.x) * kRedSlots + 1] = df_pack(o[1]);
+  bool run = grid_barrier(a.bar, epoch, a.status, &ok_sh);
+
+  double rz_old = 0.0, bbd = 0.0, rr_last = 0.0;
+  if (run) {
+    Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
+                   records_share(a.rec, gridDim.x, REC_BB, kPipeThreads)};
+    block_sum_df<kPipeThreads, 2>(v, red_sh);
+    rz_old = df_value(v[0]);
+    bbd = df_value(v[1]);
+    rr_last = bbd;
+    if (tid == 0) {
+      int stop = 1;
+      PcgState st{1, 0, PCLOTH_OK, 0, 0.0, sqrt(bbd)};
+      if (!isfinite(bbd)) {
+        st.code = PCLOTH_ERR_NONFINITE;
+        if (blockIdx.x == 0) atomicOr(a.status, ST_NONFINITE);
+      } else if (!(bbd > 0.0)) {
+        st.code = PCLOTH_OK;             // b = 0: dv = 0 is exact
+      } else if (a.maxit <= 0) {
+        st.relres = 1.0;
+        st.code = (1.0 <= a.tol2) ? PCLOTH_OK : PCLOTH_NOT_CONVERGED;
+      } else {
+        stop = 0;
+      }
+      if (stop && blockIdx.x == 0) *a.state = st;
+      stop_sh = stop;
+      // the first stages of the first SpMV
+      if (!stop)
+        for (int j = 0; j < kPipeStages && !P.ended; ++j)
+          if (producer_step<BW>(P, sh, a.m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
+    }
+    __syncthreads();
+    run = stop_sh == 0;
   }
-}
 
-// dv (padded) -> caller's float[n][3].
-__global__ void unpack_dv(int32_t n, const float4* __restrict__ dv4, float* __restrict__ out) {
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const float4 d = dv4[i];
-  out[3 * i] = d.x;
-  out[3 * i + 1] = d.y;
-  out[3 * i + 2] = d.z;
-}
+  unsigned long long t_prev = timer ? now_ns() : 0;
+  for (int32_t k = 0; run; ++k) {
+    // ---- S: q = A p, partial p.q ------------------------------------------
+    float pq = 0.f;
+    if (tid < 32) {
+      if (tid == 0 && !producer_pass<BW>(P, sh, a.m)) atomicOr(a.status, ST_WAIT_TIMEOUT);
+    } else {
+      PGather g{a.p};
+      PEpi e{a.p, a.q, 0.f};
+      if (!consumer_pass<BW>(C, sh, g, e)) atomicOr(a.status, ST_WAIT_TIMEOUT);
+      pq = e.pq;
+    }
+    {
+      Dfloat t[1] = {df_of(pq)};
+      block_sum_df<kPipeThreads, 1>(t, red_sh);
+      if (tid == 0) my_rec[REC_PQ] = df_pack(t[0]);
+    }
+    if (!grid_barrier(a.bar, epoch, a.status, &ok_sh)) break;
+    if (timer) {
+      const unsigned long long t = now_ns();
+      t_s += t - t_prev;
+      t_prev = t;
+      ++n_timed;
+    }
 
-// Closes a solve that used all its iterations (or none).
-__global__ void __launch_bounds__(kVecThreads)
-pcg_finish(int k, double tol2, const float2* __restrict__ red_rz,
-           const float2* __restrict__ red_bb, int nrz, PcgState* state) {
-  __shared__ float2 sh[33 * 2];
-  __shared__ int done_sh;
-  if (threadIdx.x == 0) done_sh = state->done;
-  __syncthreads();
-  if (done_sh) return;
-  Dfloat v[2] = {records_share(red_rz, nrz, 1, kVecThreads), records_share(red_bb, nrz, 0, kVecThreads)};
-  block_sum_df<kVecThreads, 2>(v, sh);
-  if (threadIdx.x == 0) {
-    const double rr = df_value(v[0]), bb = df_value(v[1]);
-    state->done = 1;
-    state->iterations = k;
-    state->relres = bb > 0.0 ? sqrt(rr / bb) : 0.0;
-    state->code = (rr <= tol2 * bb) ? PCLOTH_OK : PCLOTH_NOT_CONVERGED;
-    if (!isfinite(rr) || !isfinite(bb)) state->code = PCLOTH_ERR_NONFINITE;
+    // ---- U: alpha; dv, r, z; partials r.z, r.r ------------------------------
+    {
+      Dfloat v[1] = {records_share(a.rec, gridDim.x, REC_PQ, kPipeThreads)};
+      block_sum_df<kPipeThreads, 1>(v, red_sh);
+      if (tid == 0) {
+        const double pqd = df_value(v[0]);
+        int stop = 0;
+        if (!(pqd > 0.0) || !isfinite(pqd) || !isfinite(rz_old)) {
+          stop = 1;
+          const bool fin = isfinite(pqd) && isfinite(rz_old);
+          if (blockIdx.x == 0) {
+            *a.state = PcgState{1, k, fin ? PCLOTH_ERR_BREAKDOWN : PCLOTH_ERR_NONFINITE, 0,
+                                sqrt(rr_last / bbd), sqrt(bbd)};
+            atomicOr(a.status, fin ? ST_BREAKDOWN : ST_NONFINITE);
+          }
+        }
+        scal_sh = float(rz_old / pqd);
+        stop_sh = stop;
+      }
+      __syncthreads();
+    }
+    if (stop_sh) break;
+    {
+      const float alpha = scal_sh;
+      float arz = 0.f, arr = 0.f;
+      for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+        const int32_t i = own_row(f);
+        if (i >= n) continue;
+        const float4 pv = a.p[i], qv = a.q[i], rv = a.r[i], dvv = a.dv[i];
+        const float4 pu = a.pinv8[2 * int64_t(i)], pw = a.pinv8[2 * int64_t(i) + 1];
+        const float3 rn = make_float3(fmaf(-alpha, qv.x, rv.x), fmaf(-alpha, qv.y, rv.y),
+                                      fmaf(-alpha, qv.z, rv.z));
+        const float3 zn = apply_p(pu, pw, rn);
+        a.dv[i] = make_float4(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
+                              fmaf(alpha, pv.z, dvv.z), 0.f);
+        a.r[i] = make_float4(rn.x, rn.y, rn.z, 0.f);
+        a.z[i] = make_float4(zn.x, zn.y, zn.z, 0.f);
+        arz += dot3(rn, zn);
+        arr += dot3(rn, rn);
+      }
+      Dfloat o[2] = {df_of(arz), df_of(arr)};
+      block_sum_df<kPipeThreads, 2>(o, red_sh);
+      if (tid == 0) {
+        my_rec[REC_RZ] = df_pack(o[0]);
+        my_rec[REC_RR] = df_pack(o[1]);
+      }
+    }
+    if (!grid_barrier(a.bar, epoch, a.status, &ok_sh)) break;
+    if (timer) {
+      const unsigned long long t = now_ns();
+      t_u += t - t_prev;
+      t_prev = t;
+    }
+
+    // ---- P: convergence, beta, p = z + beta p ---------------------------------
+    {
+      Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
+                     records_share(a.rec, gridDim.x, REC_RR, kPipeThreads)};
+      block_sum_df<kPipeThreads, 2>(v, red_sh);
+      const double rz = df_value(v[0]), rr = df_value(v[1]);
+      if (tid == 0) {
+        const bool conv = rr <= a.tol2 * bbd;
+        const bool bad = !isfinite(rr) || !isfinite(rz) || !(rz > 0.0) || !(rz_old > 0.0);
+        int stop = 1;
+        int code = PCLOTH_OK;
+        if (conv) {
+          code = PCLOTH_OK;
+        } else if (bad) {
+          code = (isfinite(rr) && isfinite(rz)) ? PCLOTH_ERR_BREAKDOWN : PCLOTH_ERR_NONFINITE;
+          if (blockIdx.x == 0)
+            atomicOr(a.status, code == PCLOTH_ERR_BREAKDOWN ? ST_BREAKDOWN : ST_NONFINITE);
+        } else if (k + 1 >= a.maxit) {
+          code = PCLOTH_NOT_CONVERGED;
+        } else {
+          stop = 0;
+        }
+        if (stop && blockIdx.x == 0)
+          *a.state = PcgState{1, k + 1, code, 0, sqrt(rr / bbd), sqrt(bbd)};
+        scal_sh = float(rz / rz_old);
+        stop_sh = stop;
+        // the next SpMV streams the same matrix: start its first stages now
+        if (!stop)
+          for (int j = 0; j < kPipeStages && !P.ended; ++j)
+            if (producer_step<BW>(P, sh, a.m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
+      }
+      __syncthreads();
+      rr_last = rr;
+      rz_old = rz;
+    }
+    if (stop_sh) break;
+    {
+      const float beta = scal_sh;
+      for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+        const int32_t i = own_row(f);
+        if (i >= n) continue;
+        const float4 zv = a.z[i], pv = a.p[i];
+        a.p[i] = make_float4(fmaf(beta, pv.x, zv.x), fmaf(beta, pv.y, zv.y),
+                             fmaf(beta, pv.z, zv.z), 0.f);
+      }
+    }
+    if (!grid_barrier(a.bar, epoch, a.status, &ok_sh)) break;
+    if (timer) {
+      const unsigned long long t = now_ns();
+      t_p += t - t_prev;
+      t_prev = t;
+    }
+  }
+
+  // ---- copies still in flight (only after a timeout), timers, dv out -------
+  if (tid == 0) {
+    producer_drain(P, sh);
+    if (timer) {
+      a.phase_ns[0] = t_s;
+      a.phase_ns[1] = t_u;
+      a.phase_ns[2] = t_p;
+      a.phase_ns[3] = n_timed;
+    }
+  }
+  for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+    const int32_t i = own_row(f);
+    if (i >= n) continue;
+    const float4 d = a.dv[i];
+    a.dv_out[3 * int64_t(i)] = d.x;
+    a.dv_out[3 * int64_t(i) + 1] = d.y;
+    a.dv_out[3 * int64_t(i) + 2] = d.z;
   }
 }
 
@@ -193,7 +386,53 @@ state_update(int64_t m, float* __restrict__ x, float* __restrict__ v,
   if (!ok) atomicOr(status, ST_NONFINITE);
 }
 
+bool g_loop_attr[2][64] = {};
+
+template <int BW>
+int loop_attrs(int device) {
+  const int w = BW == kSymBlock ? 0 : 1;
+  if (device >= 0 && device < 64 && g_loop_attr[w][device]) return 0;
+  constexpr size_t smem = Pipe<BW>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(pcg_loop<BW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(smem));
+  if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
+    e = cudaFuncSetAttribute(pcg_loop<BW>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             pipe_carveout_percent(smem));
+  if (e != cudaSuccess) return int(e);
+  if (device >= 0 && device < 64) g_loop_attr[w][device] = true;
+  return 0;
+}
+
+// Grid of the persistent kernel: the streaming grid, capped at the CTAs
+// that can be resident at once.
+template <int BW>
+int loop_grid_for(int32_t n, int device, int sm_count, int* grid) {
+  const int e = loop_attrs<BW>(device);
+  if (e != 0) return e;
+  int per_sm = 0;
+  const cudaError_t o = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, pcg_loop<BW>, kPipeThreads, Pipe<BW>::kSmem);
+  if (o != cudaSuccess) return int(o);
+  if (per_sm <= 0) return int(cudaErrorCooperativeLaunchTooLarge);
+  *grid = std::min(spmv_grid_for(n, sm_count), per_sm * sm_count);
+  return 0;
+}
+
+// Enqueues the persistent solve (cooperative launch) on `stream`.
+template <int BW>
+cudaError_t launch_loop(const LoopArgs& a, int grid, cudaStream_t stream) {
+  LoopArgs args = a;
+  void* params[] = {&args};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(pcg_loop<BW>), dim3(grid),
+                                     dim3(kPipeThreads), params, Pipe<BW>::kSmem, stream);
+}
+
 }  // namespace
+
+int pcg_loop_grid(int blk, int32_t n, int device, int sm_count, int* grid) {
+  return blk == kSymBlock ? loop_grid_for<kSymBlock>(n, device, sm_count, grid)
+                          : loop_grid_for<9>(n, device, sm_count, grid);
+}
 
 int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt) {
   state_update<<<h->vec_grid, kVecThreads, 0, h->stream>>>(int64_t(h->n) * 3, x, v, dv, dt,
@@ -205,97 +444,39 @@ int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt
 int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iterations,
               double* rel_residual) {
   cudaStream_t s = h->stream;
-  float4* dv = h->dv4;  // padded; unpacked into dv_out at the end
-  const double tol2 = tol * tol;
   const bool prof = h->prof.on;
-  const int vg = h->vec_grid;
+  LoopArgs a{};
+  a.m = PipeMatrix{h->n, (h->n + kPipeRows - 1) / kPipeRows, h->rowptr, h->colind, h->vals};
+  a.b = h->rhs;
+  a.pinv8 = h->pinv8;
+  a.dv = h->dv4;
+  a.r = h->r4;
+  a.z = h->z4;
+  a.p = h->p4;
+  a.q = h->q4;
+  a.rec = h->rec;
+  a.bar = h->bar;
+  a.state = h->state;
+  a.status = h->d_status;
+  a.dv_out = dv_out;
+  a.phase_ns = prof ? h->phase_ns : nullptr;
+  a.tol2 = tol * tol;
+  a.maxit = maxit;
+  cudaError_t e = cudaMemsetAsync(h->bar, 0, sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "pcg barrier reset");
   if (prof) cudaEventRecord(h->ev[2], s);
-  pcg_init<<<vg, kVecThreads, 0, s>>>(h->n, h->rhs, h->pinv8, h->r4, h->z4, dv, h->p4[1],
-                                      h->red_upd[0], h->red_init, h->state);
+  e = h->blk == kSymBlock ? launch_loop<kSymBlock>(a, h->loop_grid, s)
+                          : launch_loop<9>(a, h->loop_grid, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "pcg launch");
   h->launches += 1;
-  int rc = check_launch(h, "pcg init");
-  if (rc != PCLOTH_OK) return rc;
-
-  int32_t k = 0;
-  int chunk_id = 0, pending = -1;
-  h->prof_done_at = INT32_MAX;
-  bool done = false;
-  const int per = 2 * h->chunk + 1;  // events per chunk slot
-  // Profiling mode 1 times the first iteration of every chunk (events around
-  // its two launches); mode 2 times every iteration.  Iterations enqueued
-  // after convergence return at once and are not counted.
-  const bool every = h->prof.mode == 2;
-  auto consume = [&](int slot, int launched) {
-    if (!prof || launched <= 0) return;
-    cudaEvent_t* ev = h->pev.data() + size_t(slot) * per;
-    const int timed = every ? launched : 1;
-    const int32_t first_k = h->prof_chunk_k[slot];
-    for (int j = 0; j < timed; ++j) {
-      if (first_k + j >= h->prof_done_at) break;   // launches from here on were no-ops
-      float a = 0.f, b = 0.f;
-      if (cudaEventElapsedTime(&a, ev[2 * j], ev[2 * j + 1]) == cudaSuccess &&
-          cudaEventElapsedTime(&b, ev[2 * j + 1], ev[2 * j + 2]) == cudaSuccess) {
-        h->prof.spmv_ms += a;
-        h->prof.update_ms += b;
-        h->prof.samples += 1;
-      }
-    }
-  };
-  int launched_in[2] = {0, 0};
-  while (k < maxit && !done) {
-    const int slot = chunk_id & 1;
-    const int m = std::min<int32_t>(h->chunk, maxit - k);
-    cudaEvent_t* ev = h->pev.data() + size_t(slot) * per;
-    h->prof_chunk_k[slot] = k;
-    for (int j = 0; j < m; ++j, ++k) {
-      const bool rec = prof && (every || j == 0);
-      if (rec && j == 0) cudaEventRecord(ev[0], s);
-      rc = launch_spmv_pcg(h, k, tol);
-      if (rc != PCLOTH_OK) return rc;
-      if (rec) cudaEventRecord(ev[2 * j + 1], s);
-      pcg_update<<<vg, kVecThreads, 0, s>>>(h->n, k, h->p4[k & 1], h->q4, h->pinv8, h->r4, h->z4, dv,
-                                            h->red_spmv, h->spmv_grid, h->red_upd[k & 1],
-                                            h->red_init, vg, h->red_upd[(k + 1) & 1], h->state,
-                                            h->d_status);
-      h->launches += 1;
-      if (rec) cudaEventRecord(ev[2 * j + 2], s);
-    }
-    launched_in[slot] = m;
-    rc = check_launch(h, "pcg update");
-    if (rc != PCLOTH_OK) return rc;
-    cudaMemcpyAsync(&h->state_host[slot], h->state, sizeof(PcgState), cudaMemcpyDeviceToHost, s);
-    cudaEventRecord(h->chunk_ev[slot], s);
-    if (pending >= 0) {
-      cudaError_t e = cudaEventSynchronize(h->chunk_ev[pending]);
-      if (e != cudaSuccess) return cuda_fail(h, e, "pcg poll");
-      if (h->state_host[pending].done) {
-        done = true;
-        h->prof_done_at = h->state_host[pending].iterations;
-      }
-      consume(pending, launched_in[pending]);
-    }
-    pending = slot;
-    ++chunk_id;
-  }
-  if (pending >= 0) {
-    cudaError_t e = cudaEventSynchronize(h->chunk_ev[pending]);
-    if (e != cudaSuccess) return cuda_fail(h, e, "pcg poll");
-    if (h->state_host[pending].done && h->prof_done_at > h->state_host[pending].iterations)
-      h->prof_done_at = h->state_host[pending].iterations;
-    consume(pending, launched_in[pending]);
-  }
-  pcg_finish<<<1, kVecThreads, 0, s>>>(k, tol2, h->red_upd[k & 1], h->red_init, vg, h->state);
-  h->launches += 1;
-  rc = check_launch(h, "pcg finish");
-  if (rc != PCLOTH_OK) return rc;
-  unpack_dv<<<(h->n + 255) / 256, 256, 0, s>>>(h->n, dv, dv_out);
-  h->launches += 1;
-  rc = check_launch(h, "dv unpack");
-  if (rc != PCLOTH_OK) return rc;
-  cudaMemcpyAsync(&h->state_host[0], h->state, sizeof(PcgState), cudaMemcpyDeviceToHost, s);
   if (prof) cudaEventRecord(h->ev[3], s);
-  rc = collect_status(h);  // synchronises
-  const PcgState st = h->state_host[0];
+  e = cudaMemcpyAsync(h->state_host, h->state, sizeof(PcgState), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && prof)
+    e = cudaMemcpyAsync(h->phase_host, h->phase_ns, 4 * sizeof(unsigned long long),
+                        cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "pcg state copy");
+  int rc = collect_status(h);  // synchronises
+  const PcgState st = *h->state_host;
   if (iterations) *iterations = st.iterations;
   if (rel_residual) *rel_residual = st.relres;
   if (prof) {
@@ -304,8 +485,11 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
     h->prof.solve_ms += ms;
     h->prof.solves += 1;
     h->prof.iterations += st.iterations;
-    h->prof.spmv_launches += k;
-    h->prof.update_launches += k;
+    h->prof.spmv_ms += double(h->phase_host[0]) * 1e-6;
+    h->prof.update_ms += double(h->phase_host[1] + h->phase_host[2]) * 1e-6;
+    h->prof.samples += int64_t(h->phase_host[3]);
+    h->prof.spmv_launches += st.iterations;
+    h->prof.update_launches += st.iterations;
   }
   if (rc != PCLOTH_OK && rc != PCLOTH_ERR_BREAKDOWN && rc != PCLOTH_ERR_NONFINITE) return rc;
   if (st.code != PCLOTH_OK && st.code != PCLOTH_NOT_CONVERGED) {
@@ -319,18 +503,11 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
 }
 
 // ===========================================================================
-// Allocation-free solve.
-//
-// Some callers cannot allocate GPU memory at the time they need a solve: a
-// host application (an animation tool, a game engine) that reserves the
-// GPU's memory budget for itself and forbids allocation by plug-ins, or a
-// real-time loop in which an allocation's latency, or an allocation that
-// fails in the middle of a frame, is not acceptable.  pcloth_solve_bsr3_static
-// serves them: it runs the same block-Jacobi PCG kernels as pcloth_solve on a
-// BSR3 system the caller already holds, and keeps every work vector, every
-// reduction record and the status words in one fixed array compiled into
-// this library, so it never calls cudaMalloc, cudaFree or any allocating
-// routine.
+// Allocation-free solve (pcloth_solve_bsr3_static).  It runs the same
+// persistent PCG on a general BSR3 system the caller already holds, and keeps
+// every work vector, every partial sum, the barrier counter and the status
+// words in one fixed array compiled into this library, so it never calls
+// cudaMalloc, cudaFree or any allocating routine.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it (about 2.2 MiB) until the process exits, and every call
@@ -342,12 +519,12 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
 namespace {
 
 constexpr int64_t kStaticVec = int64_t(PCLOTH_STATIC_MAX_VERTS) + 64;  // float4 per vector
-constexpr int kStaticMaxRecords = 1024;                                 // per reduction buffer
+constexpr int kStaticMaxRecords = 2048;                                 // CTAs of the solve
 constexpr size_t kStaticBytes =
     sizeof(float4) * size_t(2 * kStaticVec        // block-Jacobi inverses (2 per vertex)
-                            + 5 * kStaticVec)     // dv, r, z, q and the spare p
-    + sizeof(float4) * size_t(kStaticVec)         // second p (ping-pong)
-    + sizeof(float2) * size_t(kRedSlots) * size_t(4 * kStaticMaxRecords) + 256;
+                            + 5 * kStaticVec      // dv, r, z, p, q
+                            + kStaticVec)         // spare
+    + sizeof(float2) * size_t(kRecSlots) * size_t(kStaticMaxRecords) + 256;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
@@ -405,80 +582,56 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetSymbolAddress(scratch)");
     g_static_addr[device] = ptr;
   }
-  // A stack handle pointing into the fixed array and the caller's buffers:
-  // its containers stay empty and nothing in it is allocated or freed.
-  Handle h;
-  h.device = device;
-  h.stream = stream;
-  h.n = n;
-  h.chunk = 32;
-  cudaDeviceGetAttribute(&h.sm_count, cudaDevAttrMultiProcessorCount, device);
-  if (h.sm_count <= 0) h.sm_count = 1;
-  h.spmv_grid = spmv_grid_for(n, h.sm_count);
-  h.vec_grid = int(std::min<int64_t>((int64_t(n) + kVecThreads - 1) / kVecThreads,
-                                     int64_t(h.sm_count) * 4));
-  if (h.spmv_grid > kStaticMaxRecords || h.vec_grid > kStaticMaxRecords)
-    return fail(nullptr, PCLOTH_ERR_CAPACITY, "too many CTAs for the fixed reduction records");
+  int sm_count = 0;
+  cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, device);
+  if (sm_count <= 0) sm_count = 1;
+  int grid = 0;
+  const int ge = pcg_loop_grid(9, n, device, sm_count, &grid);
+  if (ge != 0) return cuda_fail(nullptr, cudaError_t(ge), "pcg grid");
+  if (grid > kStaticMaxRecords)
+    return fail(nullptr, PCLOTH_ERR_CAPACITY, "too many CTAs for the fixed partial sums");
   unsigned char* base = static_cast<unsigned char*>(g_static_addr[device]);
   float4* v4 = reinterpret_cast<float4*>(base);
-  h.pinv8 = v4;
-  h.dv4 = v4 + 2 * kStaticVec;
-  h.r4 = v4 + 3 * kStaticVec;
-  h.z4 = v4 + 4 * kStaticVec;
-  h.q4 = v4 + 5 * kStaticVec;
-  h.p4[0] = v4 + 6 * kStaticVec;
-  h.p4[1] = v4 + 7 * kStaticVec;
   float2* rec = reinterpret_cast<float2*>(v4 + 8 * kStaticVec);
-  h.red_spmv = rec;
-  h.red_upd[0] = rec + size_t(kRedSlots) * kStaticMaxRecords;
-  h.red_upd[1] = rec + size_t(2 * kRedSlots) * kStaticMaxRecords;
-  h.red_init = rec + size_t(3 * kRedSlots) * kStaticMaxRecords;
-  unsigned char* tail = reinterpret_cast<unsigned char*>(rec + size_t(4 * kRedSlots) * kStaticMaxRecords);
-  h.state = reinterpret_cast<PcgState*>(tail);
-  h.d_status = reinterpret_cast<uint32_t*>(tail + 64);
-  h.rowptr = const_cast<int32_t*>(rowptr);
-  h.colind = const_cast<int32_t*>(colind);
-  h.vals = const_cast<float*>(vals);
-  h.blk = 9;   // the caller's blocks are general row-major 3x3
-  h.rhs = const_cast<float*>(b);
+  unsigned char* tail = reinterpret_cast<unsigned char*>(rec + size_t(kRecSlots) * kStaticMaxRecords);
+  LoopArgs a{};
+  a.m = PipeMatrix{n, (n + kPipeRows - 1) / kPipeRows, rowptr, colind, vals};
+  a.b = b;
+  float4* pinv8 = v4;
+  a.pinv8 = pinv8;
+  a.dv = v4 + 2 * kStaticVec;
+  a.r = v4 + 3 * kStaticVec;
+  a.z = v4 + 4 * kStaticVec;
+  a.p = v4 + 5 * kStaticVec;
+  a.q = v4 + 6 * kStaticVec;
+  a.rec = rec;
+  a.state = reinterpret_cast<PcgState*>(tail);
+  uint32_t* status = reinterpret_cast<uint32_t*>(tail + 64);
+  a.bar = reinterpret_cast<unsigned long long*>(tail + 128);
+  a.status = status;
+  a.dv_out = dv_out;
+  a.phase_ns = nullptr;
+  a.tol2 = tol * tol;
+  a.maxit = maxit;
 
-  const int vg = h.vec_grid;
-  e = cudaMemsetAsync(h.d_status, 0, sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return cuda_fail(nullptr, e, "status reset");
-  bsr3_diag_inverse<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, vals, h.pinv8,
-                                                        h.d_status);
-  pcg_init<<<vg, kVecThreads, 0, stream>>>(n, b, h.pinv8, h.r4, h.z4, h.dv4, h.p4[1],
-                                           h.red_upd[0], h.red_init, h.state);
+  e = cudaMemsetAsync(tail, 0, 256, stream);   // state, status and barrier counter
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve reset");
+  bsr3_diag_inverse<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, vals, pinv8,
+                                                        status);
   e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_loop<9>(a, grid, stream);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve launch");
   PcgState st{};
-  int32_t k = 0;
-  while (k < maxit) {
-    const int m = std::min<int32_t>(h.chunk, maxit - k);
-    for (int j = 0; j < m; ++j, ++k) {
-      if (launch_spmv_pcg(&h, k, tol) != PCLOTH_OK) return fail(nullptr, PCLOTH_ERR_CUDA, h.err);
-      pcg_update<<<vg, kVecThreads, 0, stream>>>(n, k, h.p4[k & 1], h.q4, h.pinv8, h.r4, h.z4,
-                                                 h.dv4, h.red_spmv, h.spmv_grid,
-                                                 h.red_upd[k & 1], h.red_init, vg,
-                                                 h.red_upd[(k + 1) & 1], h.state, h.d_status);
-    }
-    e = cudaMemcpyAsync(&st, h.state, sizeof(PcgState), cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve poll");
-    if (st.done) break;
-  }
-  pcg_finish<<<1, kVecThreads, 0, stream>>>(k, tol * tol, h.red_upd[k & 1], h.red_init, vg, h.state);
-  unpack_dv<<<(n + 255) / 256, 256, 0, stream>>>(n, h.dv4, dv_out);
-  uint32_t status = 0;
-  e = cudaGetLastError();
-  if (e == cudaSuccess) e = cudaMemcpyAsync(&st, h.state, sizeof(PcgState), cudaMemcpyDeviceToHost, stream);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(&status, h.d_status, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+  uint32_t st_bits = 0;
+  e = cudaMemcpyAsync(&st, a.state, sizeof(PcgState), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&st_bits, status, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve result");
   if (iterations) *iterations = st.iterations;
   if (rel_residual) *rel_residual = st.relres;
-  if (status & ST_WAIT_TIMEOUT) return fail(nullptr, PCLOTH_ERR_CUDA, "device wait timed out");
-  if (status & ST_NONFINITE)
+  if (st_bits & ST_WAIT_TIMEOUT) return fail(nullptr, PCLOTH_ERR_CUDA, "device wait timed out");
+  if (st_bits & ST_NONFINITE)
     return fail(nullptr, PCLOTH_ERR_NONFINITE, "non-finite value or missing/singular diagonal block");
   if (st.code == PCLOTH_ERR_BREAKDOWN) return fail(nullptr, st.code, "PCG breakdown");
   if (st.code == PCLOTH_ERR_NONFINITE) return fail(nullptr, st.code, "non-finite value in PCG");

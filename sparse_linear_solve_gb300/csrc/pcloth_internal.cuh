@@ -50,16 +50,19 @@ constexpr int kAsmCap = 768;      // blocks staged per assembly group
 constexpr int kAsmThreads = 256;
 
 constexpr int kVecThreads = 256;
-constexpr int kRedSlots = 2;      // double-float (float2) slots per partial record
+// Per-CTA partial sums of the PCG dot products, one double-float (float2)
+// per slot: p.q, r.z, r.r, b.b.
+constexpr int kRecSlots = 4;
+enum { REC_PQ = 0, REC_RZ = 1, REC_RR = 2, REC_BB = 3 };
 
 // --------------------------------------------------------------- handle ----
 struct Profile {
   bool on = false;
-  int mode = 1;          // 1: first iteration of each chunk, 2: every iteration
+  int mode = 1;          // accepted for compatibility: 1 and 2 behave alike
   double assemble_ms = 0, spmv_ms = 0, update_ms = 0, solve_ms = 0;
   int64_t spmv_launches = 0, update_launches = 0, assemble_calls = 0;
   int64_t solves = 0, iterations = 0;
-  int64_t samples = 0;   // PCG iterations whose two launches were timed
+  int64_t samples = 0;   // PCG iterations whose phases were timed
 };
 
 struct Handle {
@@ -68,7 +71,6 @@ struct Handle {
   int32_t n = 0;             // vertices
   int32_t ns = 0;            // springs
   int32_t max_contacts = 0;
-  int32_t chunk = 16;        // PCG iterations per poll
   int key_bits = 1;          // bits per vertex index in a sort key
   int64_t nnzb_static = 0;
   int64_t nnzb_cap = 0;
@@ -77,6 +79,7 @@ struct Handle {
   float last_dt = 0.f;
   int sm_count = 0;
   int spmv_grid = 0, vec_grid = 0;
+  int loop_grid = 0;         // CTAs of the persistent PCG kernel (co-resident)
   int64_t launches = 0;      // kernels launched by this handle
   std::string err;
 
@@ -125,28 +128,25 @@ struct Handle {
   float* hcr = nullptr;
 
   // PCG workspace: one float4 (x, y, z, 0) per vertex, so that a gather is
-  // one aligned 16-byte load and the vector kernels are fully coalesced
+  // one aligned 16-byte load and the vector phases are fully coalesced
   float* dv = nullptr;             // float[n][3] scratch (pcloth_step without dv)
   float4* dv4 = nullptr;
   float4* r4 = nullptr;
   float4* z4 = nullptr;
-  float4* p4[2] = {nullptr, nullptr};
+  float4* p4 = nullptr;
   float4* q4 = nullptr;
-  float2* red_spmv = nullptr;      // spmv_grid records (p.q)
-  float2* red_upd[2] = {nullptr, nullptr};  // vec_grid records (r.z, r.r)
-  float2* red_init = nullptr;      // vec_grid records (b.b)
+  float2* rec = nullptr;           // loop_grid * kRecSlots partial sums
+  unsigned long long* bar = nullptr;       // grid-barrier arrival counter
+  unsigned long long* phase_ns = nullptr;  // [4] phase times of the last solve
+  unsigned long long* phase_host = nullptr;  // pinned copy
   PcgState* state = nullptr;       // device
-  PcgState* state_host = nullptr;  // pinned, 2 slots
+  PcgState* state_host = nullptr;  // pinned
   uint32_t* d_status = nullptr;    // device error bits
   uint32_t* h_status = nullptr;    // pinned copy
 
   // profiling
   Profile prof;
   cudaEvent_t ev[8] = {};
-  std::vector<cudaEvent_t> pev;   // per-launch events of two PCG chunks
-  cudaEvent_t chunk_ev[2] = {};
-  int32_t prof_chunk_k[2] = {0, 0};  // first iteration of the chunk in each slot
-  int32_t prof_done_at = 0;          // iterations that did work, once known
 };
 
 // ------------------------------------------------------------- helpers ----
@@ -169,8 +169,8 @@ int assemble_system(Handle* h, const float* x, const float* v,
 
 // spmv.cu
 int spmv_grid_for(int32_t n, int sm_count);
+int pipe_carveout_percent(size_t smem);
 int launch_spmv(Handle* h, const float* in, float* out);
-int launch_spmv_pcg(Handle* h, int k, double tol);  // k = 0-based iteration
 
 // assemble.cu: expand the packed symmetric inverses to float[n][3][3]
 int launch_pinv_expand(Handle* h, float* out9);
@@ -178,6 +178,9 @@ int launch_pinv_expand(Handle* h, float* out9);
 int launch_vals_expand(Handle* h, float* out9, int64_t nnzb);
 
 // pcg.cu
+// CTAs of the persistent PCG kernel for blocks of blk floats: the streaming
+// grid, capped at what can be co-resident (a cooperative launch needs all).
+int pcg_loop_grid(int blk, int32_t n, int device, int sm_count, int* grid);
 int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv,
               int32_t* iterations, double* rel_residual);
 int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt);
@@ -241,12 +244,14 @@ __device__ __forceinline__ void block_sum_df(Dfloat (&v)[N], float2* sh) {
   __syncthreads();
 }
 
-// Adds slot `slot` of `count` partial records (kRedSlots float2 each) that an
-// earlier kernel wrote, this thread's share in index order.
+// Adds slot `slot` of `count` partial records (kRecSlots float2 each) that
+// the CTAs of the grid wrote, this thread's share in index order.  The loads
+// bypass L1: other SMs wrote the records.
 __device__ __forceinline__ Dfloat records_share(const float2* rec, int count, int slot,
                                                 int threads) {
   Dfloat a{0.f, 0.f};
-  for (int t = threadIdx.x; t < count; t += threads) a = df_add(a, df_of(rec[t * kRedSlots + slot]));
+  for (int t = threadIdx.x; t < count; t += threads)
+    a = df_add(a, df_of(__ldcg(&rec[t * kRecSlots + slot])));
   return a;
 }
 #endif

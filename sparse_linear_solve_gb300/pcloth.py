@@ -53,7 +53,7 @@ class Springs(ctypes.Structure):
 
 class Opts(ctypes.Structure):
     _fields_ = [("max_contacts", ctypes.c_int32), ("device", ctypes.c_int),
-                ("stream", ctypes.c_void_p), ("max_iter_chunk", ctypes.c_int32)]
+                ("stream", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -139,7 +139,7 @@ def _elements(el, device, name) -> Springs:
 # ------------------------------------------------------ C-named functions --
 
 def pcloth_create(mass: torch.Tensor, gravity, springs, max_contacts: int = 0,
-                  stream: Optional[int] = None, max_iter_chunk: int = 0) -> int:
+                  stream: Optional[int] = None) -> int:
     """Create a handle (int).  mass: cuda float32[N]; springs: (i, j, k, rest)."""
     _check(mass, torch.float32, None, None, "mass")
     dev = mass.device
@@ -150,8 +150,7 @@ def pcloth_create(mass: torch.Tensor, gravity, springs, max_contacts: int = 0,
         stream = torch.cuda.current_stream(dev).cuda_stream
     g = (ctypes.c_float * 3)(*[float(x) for x in gravity])
     mesh = Mesh(int(mass.shape[0]), _ptr(mass), g)
-    opts = Opts(int(max_contacts), int(dev.index or 0), ctypes.c_void_p(stream),
-                int(max_iter_chunk))
+    opts = Opts(int(max_contacts), int(dev.index or 0), ctypes.c_void_p(stream))
     out = ctypes.c_void_p()
     rc = lib().pcloth_create(ctypes.byref(mesh), ctypes.byref(sp), ctypes.byref(opts),
                              ctypes.byref(out))
@@ -256,7 +255,8 @@ def pcloth_destroy(h: int):
 
 
 def pcloth_profile_enable(h: int, on=True):
-    """on: 0/False off, 1/True sample one iteration per chunk, 2 every iteration."""
+    """on: 0/False off; any other value times assemblies, PCG launches and the
+    PCG kernel's phases."""
     rc = lib().pcloth_profile_enable(h, int(on))
     if rc != OK:
         _raise(h, rc)
@@ -318,7 +318,7 @@ class PCloth:
     """One cloth on one GPU: owns a libpcloth handle and keeps inputs alive."""
 
     def __init__(self, mass, gravity, springs, max_contacts: int = 0,
-                 device="cuda", stream: Optional[int] = None, max_iter_chunk: int = 0):
+                 device="cuda", stream: Optional[int] = None):
         device = torch.device(device)
         if device.type == "cuda" and device.index is None:
             device = torch.device("cuda", torch.cuda.current_device())
@@ -326,8 +326,7 @@ class PCloth:
         self.mass = _dev_tensor(mass, torch.float32, device)
         self.n = int(self.mass.shape[0])
         self.springs = to_device_elements(springs, device)
-        self.h = pcloth_create(self.mass, gravity, self.springs, max_contacts, stream,
-                               max_iter_chunk)
+        self.h = pcloth_create(self.mass, gravity, self.springs, max_contacts, stream)
         self._contacts = None
 
     @classmethod

@@ -14,8 +14,8 @@ def to_dev(a, dtype=torch.float32):
     return torch.from_numpy(np.ascontiguousarray(a)).to(device=DEV, dtype=dtype)
 
 
-def make(w, chunk=0):
-    return pc.PCloth.from_workload(w, device=DEV, max_iter_chunk=chunk)
+def make(w):
+    return pc.PCloth.from_workload(w, device=DEV)
 
 
 def block_rel_err(vals_gpu, vals_ref):
