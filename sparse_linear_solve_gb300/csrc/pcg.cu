@@ -126,9 +126,10 @@ struct PEpi {
   const float4* p;
   float4* q;
   float pq;
+  float4 pr;   // p of this thread's row, loaded when its tile starts
+  __device__ __forceinline__ void begin(int32_t row) { pr = p[row]; }
   __device__ __forceinline__ void operator()(int32_t row, float3 acc) {
     q[row] = make_float4(acc.x, acc.y, acc.z, 0.f);
-    const float4 pr = p[row];
     pq = fmaf(pr.x, acc.x, fmaf(pr.y, acc.y, fmaf(pr.z, acc.z, pq)));
   }
 };
@@ -156,7 +157,7 @@ pcg_loop(LoopArgs a) {
   unsigned long long t_s = 0, t_u = 0, t_p = 0, n_timed = 0;
   Producer P;
   Consumer C;
-  producer_begin(P);
+  if (tid == 0) producer_begin(P, a.m);
   consumer_begin(C);
 
   // ---- init: r = b, z = P b, dv = 0, p = z; partials r.z and b.b ---------
@@ -226,7 +227,7 @@ pcg_loop(LoopArgs a) {
       if (tid == 0 && !producer_pass<BW>(P, sh, a.m)) atomicOr(a.status, ST_WAIT_TIMEOUT);
     } else {
       PGather g{a.p};
-      PEpi e{a.p, a.q, 0.f};
+      PEpi e{a.p, a.q, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
       if (!consumer_pass<BW>(C, sh, g, e)) atomicOr(a.status, ST_WAIT_TIMEOUT);
       pq = e.pq;
     }

@@ -22,6 +22,7 @@ struct PlainGather {
 
 struct PlainEpi {
   float* out;
+  __device__ __forceinline__ void begin(int32_t) const {}
   __device__ __forceinline__ void operator()(int32_t row, float3 acc) const {
     const int64_t g3 = int64_t(row) * 3;
     out[g3] = acc.x;
@@ -41,7 +42,7 @@ spmv_plain(PipeMatrix m, const float* __restrict__ in, float* __restrict__ out,
   if (threadIdx.x < 32) {
     if (threadIdx.x == 0) {
       Producer P;
-      producer_begin(P);
+      producer_begin(P, m);
       if (!producer_pass<BW>(P, sh, m)) atomicOr(status, ST_WAIT_TIMEOUT);
     }
   } else {

@@ -168,17 +168,34 @@ struct Producer {
   int s;
   uint32_t ph;
   int32_t tile, c0;
+  int32_t b1;            // end block of the current tile
+  int32_t nb0, nb1;      // block range of the next tile to start (loaded ahead)
   bool ended;
   uint32_t used, last_ph;
   uint64_t pol;
 };
+
+// Block range [rowptr[r0], rowptr[r0 + rows]) of a tile; loads issued here
+// are consumed a stage or more later, so their latency is off the path.
+__device__ __forceinline__ void tile_bounds_of(const PipeMatrix& m, int32_t tile, int32_t& b0,
+                                               int32_t& b1) {
+  if (tile < m.ntiles) {
+    const int32_t r0 = tile * kPipeRows;
+    b0 = m.rowptr[r0];
+    b1 = m.rowptr[min(r0 + kPipeRows, m.n)];
+  } else {
+    b0 = b1 = 0;
+  }
+}
 static_assert(kPipeStages <= 32, "slot bit masks");
 
-__device__ __forceinline__ void producer_begin(Producer& P) {
+__device__ __forceinline__ void producer_begin(Producer& P, const PipeMatrix& m) {
   P.s = 0;
   P.ph = 0;
   P.tile = blockIdx.x;
   P.c0 = -1;
+  P.b1 = 0;
+  tile_bounds_of(m, P.tile, P.nb0, P.nb1);
   P.ended = false;
   P.used = 0;
   P.last_ph = 0;
@@ -206,15 +223,22 @@ __device__ __forceinline__ int producer_step(Producer& P, const PipeShared& sh,
   if (P.tile >= m.ntiles) {
     sh.desc[P.s].tile = -1;   // end marker: a plain arrival, no bytes
     mbar_arrive(&sh.full[P.s]);
-    P.tile = blockIdx.x;
+    P.tile = blockIdx.x;      // the next pass starts over
     P.c0 = -1;
+    tile_bounds_of(m, P.tile, P.nb0, P.nb1);
     P.ended = true;
     ret = 0;
   } else {
     const int32_t r0 = P.tile * kPipeRows;
     const int32_t nrows = min(kPipeRows, m.n - r0);
-    const int32_t b0 = m.rowptr[r0], b1 = m.rowptr[r0 + nrows];
-    const int32_t c0 = P.c0 < 0 ? b0 : P.c0;
+    const bool first = P.c0 < 0;
+    if (first) {              // start of a tile: its bounds were loaded ahead
+      P.b1 = P.nb1;
+      P.c0 = P.nb0;
+      tile_bounds_of(m, P.tile + int32_t(gridDim.x), P.nb0, P.nb1);
+    }
+    const int32_t b1 = P.b1;
+    const int32_t c0 = P.c0;
     const int32_t c1 = min(b1, c0 + kPipeCap);
     unsigned char* st = sh.stages + size_t(P.s) * Pipe<BW>::kStageBytes;
     const int64_t va0 = (int64_t(c0) * (4 * BW)) & ~int64_t(15);
@@ -227,7 +251,7 @@ __device__ __forceinline__ int producer_step(Producer& P, const PipeShared& sh,
     d.tile = P.tile; d.r0 = r0; d.nrows = nrows; d.c0 = c0; d.c1 = c1;
     d.voff = int32_t((int64_t(c0) * (4 * BW) - va0) >> 2);
     d.coff = int32_t((int64_t(c0) * 4 - ca0) >> 2);
-    d.flags = (c0 == b0 ? 1 : 0) | (c1 == b1 ? 2 : 0);
+    d.flags = (first ? 1 : 0) | (c1 == b1 ? 2 : 0);
     sh.desc[P.s] = d;
     mbar_arrive_expect_tx(&sh.full[P.s], rp_bytes + v_bytes + c_bytes);
     bulk_g2s(st, m.rowptr + r0, rp_bytes, &sh.full[P.s], P.pol);
@@ -276,8 +300,9 @@ __device__ __forceinline__ void consumer_begin(Consumer& C) {
 
 // Consumer side of one pass (threads 32 .. kPipeThreads-1): processes stages
 // up to and including the end marker.  gather(col) returns the input vertex
-// col as a float3; epi(row, acc) receives each finished row's sum.  Returns
-// false if a stage never arrived.
+// col as a float3; epi.begin(row) is called when a tile starts (before the
+// gathers, so loads it issues overlap them) and epi(row, acc) receives each
+// finished row's sum.  Returns false if a stage never arrived.
 template <int BW, class Gather, class Epi>
 __device__ __forceinline__ bool consumer_pass(Consumer& C, const PipeShared& sh, Gather& gather,
                                               Epi& epi) {
@@ -298,6 +323,8 @@ __device__ __forceinline__ bool consumer_pass(Consumer& C, const PipeShared& sh,
         reinterpret_cast<const int32_t*>(st + kPipeRpInts * 4 + Pipe<BW>::kValBytes) + d.coff;
     float4* part = sh.parts + C.buf * kPipeCap;
     const int32_t cn = d.c1 - d.c0;
+    const bool row_owner = ct < d.nrows;
+    if (row_owner && (d.flags & 1)) epi.begin(d.r0 + ct);
     // phase B: block products, all of a thread's gathers in flight at once
     {
       int32_t col[kPipePerThread];
@@ -318,7 +345,6 @@ __device__ __forceinline__ bool consumer_pass(Consumer& C, const PipeShared& sh,
     }
     named_barrier_sync(1, kPipeConsumers);
     // phase C: row sums in column order, one thread per row
-    const bool row_owner = ct < d.nrows;
     if (row_owner) {
       const int32_t rs = max(rp[ct], d.c0) - d.c0, re = min(rp[ct + 1], d.c1) - d.c0;
       for (int32_t j = rs; j < re; ++j) {
