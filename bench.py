@@ -252,16 +252,16 @@ def run_ours(args, rank, world, local_rank):
     # ---- roofline of the dominant kernel: the persistent PCG -------------
     # Algorithmic bytes per PCG iteration: the matrix once (28 B/block:
     # 24 packed symmetric values + 4 colind; 4 B/row rowptr), p read once and
-    # q written (24 B/row), the update phase (dv, p, q, r read, the
-    # symmetric P read 24 B, dv, r, z written: 108 B/row) and the
-    # direction update (z, p read, p written: 36 B/row).  Per launch: that
-    # times the iterations, plus the start (b 12, P 24 read; r, z, p, dv
-    # written 48) and dv out (12 + 12) = 108 B/row.
+    # q written (24 B/row), the update phase (q, r read, the symmetric P read
+    # 24 B, r, z written: 72 B/row) and the direction phase (p, dv, z read,
+    # dv, p written: 60 B/row).  Per launch: that times the iterations, plus
+    # the start (b 12, P 24 read; r, z, p, dv written 48) and dv out
+    # (12 + 12) = 108 B/row.
     n = w.n_verts
     nnzb = nnzb_seen[-1]
-    it_bytes = 28 * nnzb + 172 * n
+    it_bytes = 28 * nnzb + 160 * n
     spmv_bytes = 28 * nnzb + 28 * n
-    vec_bytes = 144 * n
+    vec_bytes = 132 * n
     iters = max(prof["iterations"], 1)
     solves = max(prof["solves"], 1)
     launch_bytes = (iters * it_bytes + solves * 108 * n) / solves
@@ -330,9 +330,9 @@ def run_ours(args, rank, world, local_rank):
                       achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
                       peak_source=peak_src, bytes_per_launch=launch_bytes,
                       bytes_model="per iteration 28 B/block (24 packed symmetric values + "
-                                  "4 colind) + 172 B/row (rowptr 4; SpMV p 12 read, q 12 "
-                                  "written; update dv p q r 48 + P 24 read, dv r z 36 "
-                                  "written; direction z p 24 read, p 12 written); per launch "
+                                  "4 colind) + 160 B/row (rowptr 4; SpMV p 12 read, q 12 "
+                                  "written; update q r 24 + P 24 read, r z 24 written; "
+                                  "direction p dv z 36 read, dv p 24 written); per launch "
                                   "+108 B/row (start and dv out)",
                       traffic=(None if stored_traffic(kernel_source_digest()) is None else
                                stored_traffic(kernel_source_digest()) * iters / solves)),

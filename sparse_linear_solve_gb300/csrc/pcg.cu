@@ -11,10 +11,12 @@
 //
 //   S  q = A p (the streaming SpMV of spmv_pipe.cuh, gathering p only);
 //      partial p.q over the CTA's rows                              barrier
-//   U  alpha = r.z / p.q; dv += alpha p; r -= alpha q; z = P r;
-//      partials r.z and r.r                                         barrier
-//   P  stop if |r| <= tol |b| (or breakdown, or maxit); otherwise
-//      beta = r.z / r.z_old and p = z + beta p                      barrier
+//   U  alpha = r.z / p.q; r -= alpha q; z = P r; partials r.z, r.r  barrier
+//   P  dv += alpha p; stop if |r| <= tol |b| (or breakdown, or maxit);
+//      otherwise beta = r.z / r.z_old and p = z + beta p            barrier
+//
+// (dv is updated in P rather than U: both it and the new direction read the
+// same p, so each row's p is read once per iteration.)
 //
 // Every scalar is formed by every CTA from the same per-CTA partials in the
 // same order (double-float sums), so all CTAs take the same decisions and
@@ -31,8 +33,20 @@
 
 #include "spmv_pipe.cuh"
 
+
 namespace pcloth_impl {
 namespace {
+
+// Accesses of the solver's vectors (p, q, r, z, dv, P: about 93 MB on the
+// largest cloth, less than L2) carry an L2 evict-last policy, so that the
+// matrix streamed past them (evict-first) does not push them out.
+struct Vec {
+  uint64_t pol;
+  __device__ __forceinline__ float4 ld(const float4* p) const { return ld_policy(p, pol); }
+  __device__ __forceinline__ void st(float4* p, float4 v) const { st_policy(p, v, pol); }
+};
+
+__device__ __forceinline__ Vec vec_access() { return Vec{policy_evict_last()}; }
 
 __device__ __forceinline__ float3 apply_p(float4 u, float4 w, float3 r) {
   // P = [[u.x u.y u.z] [u.y u.w w.x] [u.z w.x w.y]]
@@ -116,8 +130,9 @@ __device__ __forceinline__ int32_t own_row(int32_t f) {
 
 struct PGather {
   const float4* p;
+  Vec vm;
   __device__ __forceinline__ float3 operator()(int32_t col) const {
-    const float4 v = p[col];
+    const float4 v = vm.ld(p + col);
     return make_float3(v.x, v.y, v.z);
   }
 };
@@ -125,13 +140,24 @@ struct PGather {
 struct PEpi {
   const float4* p;
   float4* q;
+  Vec vm;
   float pq;
   float4 pr;   // p of this thread's row, loaded when its tile starts
-  __device__ __forceinline__ void begin(int32_t row) { pr = p[row]; }
+  __device__ __forceinline__ void begin(int32_t row) { pr = vm.ld(p + row); }
   __device__ __forceinline__ void operator()(int32_t row, float3 acc) {
-    q[row] = make_float4(acc.x, acc.y, acc.z, 0.f);
+    vm.st(q + row, make_float4(acc.x, acc.y, acc.z, 0.f));
     pq = fmaf(pr.x, acc.x, fmaf(pr.y, acc.y, fmaf(pr.z, acc.z, pq)));
   }
+};
+
+// State that only thread 0 of a CTA uses (the producer lane, the grid
+// barrier, the scalar decisions, the phase timers), kept in shared memory so
+// that it takes no registers in the other threads.  Thread 0 copies the
+// producer's cursor into registers for each stretch of stage issues.
+struct Lead {
+  Producer P;
+  unsigned long long epoch, t_s, t_u, t_p, n_timed, t_prev;
+  double rz_old, bbd, rr_last;
 };
 
 template <int BW>
@@ -143,6 +169,7 @@ pcg_loop(LoopArgs a) {
   __shared__ int ok_sh;
   __shared__ int stop_sh;
   __shared__ float scal_sh;
+  __shared__ Lead L;
   pipe_init(sh);
   __syncthreads();
 
@@ -153,11 +180,11 @@ pcg_loop(LoopArgs a) {
   const int32_t nslots = my_tiles * kPipeRows;
   float2* my_rec = a.rec + size_t(blockIdx.x) * kRecSlots;
   const bool timer = a.phase_ns != nullptr && blockIdx.x == 0 && tid == 0;
-  unsigned long long epoch = 0;
-  unsigned long long t_s = 0, t_u = 0, t_p = 0, n_timed = 0;
-  Producer P;
   Consumer C;
-  if (tid == 0) producer_begin(P, a.m);
+  if (tid == 0) {
+    producer_begin(L.P, a.m);
+    L.epoch = L.t_s = L.t_u = L.t_p = L.n_timed = L.t_prev = 0;
+  }
   consumer_begin(C);
 
   // ---- init: r = b, z = P b, dv = 0, p = z; partials r.z and b.b ---------
@@ -184,17 +211,17 @@ pcg_loop(LoopArgs a) {
       my_rec[REC_BB] = df_pack(v[1]);
     }
   }
-  bool run = grid_barrier(a.bar, epoch, a.status, &ok_sh);
+  bool run = grid_barrier(a.bar, L.epoch, a.status, &ok_sh);
 
-  double rz_old = 0.0, bbd = 0.0, rr_last = 0.0;
   if (run) {
     Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
                    records_share(a.rec, gridDim.x, REC_BB, kPipeThreads)};
     block_sum_df<kPipeThreads, 2>(v, red_sh);
-    rz_old = df_value(v[0]);
-    bbd = df_value(v[1]);
-    rr_last = bbd;
     if (tid == 0) {
+      const double bbd = df_value(v[1]);
+      L.rz_old = df_value(v[0]);
+      L.bbd = bbd;
+      L.rr_last = bbd;
       int stop = 1;
       PcgState st{1, 0, PCLOTH_OK, 0, 0.0, sqrt(bbd)};
       if (!isfinite(bbd)) {
@@ -211,23 +238,31 @@ pcg_loop(LoopArgs a) {
       if (stop && blockIdx.x == 0) *a.state = st;
       stop_sh = stop;
       // the first stages of the first SpMV
-      if (!stop)
+      if (!stop) {
+        Producer P = L.P;
         for (int j = 0; j < kPipeStages && !P.ended; ++j)
           if (producer_step<BW>(P, sh, a.m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
+        L.P = P;
+      }
     }
     __syncthreads();
     run = stop_sh == 0;
   }
 
-  unsigned long long t_prev = timer ? now_ns() : 0;
+  if (timer) L.t_prev = now_ns();
   for (int32_t k = 0; run; ++k) {
     // ---- S: q = A p, partial p.q ------------------------------------------
     float pq = 0.f;
     if (tid < 32) {
-      if (tid == 0 && !producer_pass<BW>(P, sh, a.m)) atomicOr(a.status, ST_WAIT_TIMEOUT);
+      if (tid == 0) {
+        Producer P = L.P;
+        if (!producer_pass<BW>(P, sh, a.m)) atomicOr(a.status, ST_WAIT_TIMEOUT);
+        L.P = P;
+      }
     } else {
-      PGather g{a.p};
-      PEpi e{a.p, a.q, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+      const Vec vm = vec_access();
+      PGather g{a.p, vm};
+      PEpi e{a.p, a.q, vm, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
       if (!consumer_pass<BW>(C, sh, g, e)) atomicOr(a.status, ST_WAIT_TIMEOUT);
       pq = e.pq;
     }
@@ -236,27 +271,27 @@ pcg_loop(LoopArgs a) {
       block_sum_df<kPipeThreads, 1>(t, red_sh);
       if (tid == 0) my_rec[REC_PQ] = df_pack(t[0]);
     }
-    if (!grid_barrier(a.bar, epoch, a.status, &ok_sh)) break;
+    if (!grid_barrier(a.bar, L.epoch, a.status, &ok_sh)) break;
     if (timer) {
       const unsigned long long t = now_ns();
-      t_s += t - t_prev;
-      t_prev = t;
-      ++n_timed;
+      L.t_s += t - L.t_prev;
+      L.t_prev = t;
+      ++L.n_timed;
     }
 
-    // ---- U: alpha; dv, r, z; partials r.z, r.r ------------------------------
+    // ---- U: alpha; r, z; partials r.z, r.r ----------------------------------
     {
       Dfloat v[1] = {records_share(a.rec, gridDim.x, REC_PQ, kPipeThreads)};
       block_sum_df<kPipeThreads, 1>(v, red_sh);
       if (tid == 0) {
-        const double pqd = df_value(v[0]);
+        const double pqd = df_value(v[0]), rz_old = L.rz_old, bbd = L.bbd;
         int stop = 0;
         if (!(pqd > 0.0) || !isfinite(pqd) || !isfinite(rz_old)) {
           stop = 1;
           const bool fin = isfinite(pqd) && isfinite(rz_old);
           if (blockIdx.x == 0) {
             *a.state = PcgState{1, k, fin ? PCLOTH_ERR_BREAKDOWN : PCLOTH_ERR_NONFINITE, 0,
-                                sqrt(rr_last / bbd), sqrt(bbd)};
+                                sqrt(L.rr_last / bbd), sqrt(bbd)};
             atomicOr(a.status, fin ? ST_BREAKDOWN : ST_NONFINITE);
           }
         }
@@ -266,21 +301,20 @@ pcg_loop(LoopArgs a) {
       __syncthreads();
     }
     if (stop_sh) break;
+    const float alpha = scal_sh;
+    const Vec vm = vec_access();
     {
-      const float alpha = scal_sh;
       float arz = 0.f, arr = 0.f;
       for (int32_t f = tid; f < nslots; f += kPipeThreads) {
         const int32_t i = own_row(f);
-        if (i >= n) continue;
-        const float4 pv = a.p[i], qv = a.q[i], rv = a.r[i], dvv = a.dv[i];
-        const float4 pu = a.pinv8[2 * int64_t(i)], pw = a.pinv8[2 * int64_t(i) + 1];
+        if (i >= n) break;   // rows grow with f: the rest are past the end too
+        const float4 qv = vm.ld(a.q + i), rv = vm.ld(a.r + i);
+        const float4 pu = vm.ld(a.pinv8 + 2 * int64_t(i)), pw = vm.ld(a.pinv8 + 2 * int64_t(i) + 1);
         const float3 rn = make_float3(fmaf(-alpha, qv.x, rv.x), fmaf(-alpha, qv.y, rv.y),
                                       fmaf(-alpha, qv.z, rv.z));
         const float3 zn = apply_p(pu, pw, rn);
-        a.dv[i] = make_float4(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
-                              fmaf(alpha, pv.z, dvv.z), 0.f);
-        a.r[i] = make_float4(rn.x, rn.y, rn.z, 0.f);
-        a.z[i] = make_float4(zn.x, zn.y, zn.z, 0.f);
+        vm.st(a.r + i, make_float4(rn.x, rn.y, rn.z, 0.f));
+        vm.st(a.z + i, make_float4(zn.x, zn.y, zn.z, 0.f));
         arz += dot3(rn, zn);
         arr += dot3(rn, rn);
       }
@@ -291,20 +325,21 @@ pcg_loop(LoopArgs a) {
         my_rec[REC_RR] = df_pack(o[1]);
       }
     }
-    if (!grid_barrier(a.bar, epoch, a.status, &ok_sh)) break;
+    if (!grid_barrier(a.bar, L.epoch, a.status, &ok_sh)) break;
     if (timer) {
       const unsigned long long t = now_ns();
-      t_u += t - t_prev;
-      t_prev = t;
+      L.t_u += t - L.t_prev;
+      L.t_prev = t;
     }
 
-    // ---- P: convergence, beta, p = z + beta p ---------------------------------
+    // ---- P: convergence, beta; dv += alpha p, p = z + beta p ------------------
     {
       Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
                      records_share(a.rec, gridDim.x, REC_RR, kPipeThreads)};
       block_sum_df<kPipeThreads, 2>(v, red_sh);
-      const double rz = df_value(v[0]), rr = df_value(v[1]);
       if (tid == 0) {
+        const double rz = df_value(v[0]), rr = df_value(v[1]);
+        const double rz_old = L.rz_old, bbd = L.bbd;
         const bool conv = rr <= a.tol2 * bbd;
         const bool bad = !isfinite(rr) || !isfinite(rz) || !(rz > 0.0) || !(rz_old > 0.0);
         int stop = 1;
@@ -324,42 +359,53 @@ pcg_loop(LoopArgs a) {
           *a.state = PcgState{1, k + 1, code, 0, sqrt(rr / bbd), sqrt(bbd)};
         scal_sh = float(rz / rz_old);
         stop_sh = stop;
+        L.rr_last = rr;
+        L.rz_old = rz;
         // the next SpMV streams the same matrix: start its first stages now
-        if (!stop)
+        if (!stop) {
+          Producer P = L.P;
           for (int j = 0; j < kPipeStages && !P.ended; ++j)
             if (producer_step<BW>(P, sh, a.m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
+          L.P = P;
+        }
       }
       __syncthreads();
-      rr_last = rr;
-      rz_old = rz;
     }
-    if (stop_sh) break;
+    // dv += alpha p_k (every exit from here on keeps it), then, to go on,
+    // p_{k+1} = z_{k+1} + beta p_k
+    const bool stop = stop_sh != 0;
     {
       const float beta = scal_sh;
       for (int32_t f = tid; f < nslots; f += kPipeThreads) {
         const int32_t i = own_row(f);
-        if (i >= n) continue;
-        const float4 zv = a.z[i], pv = a.p[i];
-        a.p[i] = make_float4(fmaf(beta, pv.x, zv.x), fmaf(beta, pv.y, zv.y),
-                             fmaf(beta, pv.z, zv.z), 0.f);
+        if (i >= n) break;
+        const float4 pv = vm.ld(a.p + i), dvv = vm.ld(a.dv + i);
+        vm.st(a.dv + i, make_float4(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
+                                    fmaf(alpha, pv.z, dvv.z), 0.f));
+        if (!stop) {
+          const float4 zv = vm.ld(a.z + i);
+          vm.st(a.p + i, make_float4(fmaf(beta, pv.x, zv.x), fmaf(beta, pv.y, zv.y),
+                                     fmaf(beta, pv.z, zv.z), 0.f));
+        }
       }
     }
-    if (!grid_barrier(a.bar, epoch, a.status, &ok_sh)) break;
+    if (stop) break;
+    if (!grid_barrier(a.bar, L.epoch, a.status, &ok_sh)) break;
     if (timer) {
       const unsigned long long t = now_ns();
-      t_p += t - t_prev;
-      t_prev = t;
+      L.t_p += t - L.t_prev;
+      L.t_prev = t;
     }
   }
 
   // ---- copies still in flight (only after a timeout), timers, dv out -------
   if (tid == 0) {
-    producer_drain(P, sh);
+    producer_drain(L.P, sh);
     if (timer) {
-      a.phase_ns[0] = t_s;
-      a.phase_ns[1] = t_u;
-      a.phase_ns[2] = t_p;
-      a.phase_ns[3] = n_timed;
+      a.phase_ns[0] = L.t_s;
+      a.phase_ns[1] = L.t_u;
+      a.phase_ns[2] = L.t_p;
+      a.phase_ns[3] = L.n_timed;
     }
   }
   for (int32_t f = tid; f < nslots; f += kPipeThreads) {
