@@ -21,9 +21,10 @@
 // Every scalar is formed by every CTA from the same per-CTA partials in the
 // same order (double-float sums), so all CTAs take the same decisions and
 // the solve is bitwise reproducible.  No host round trip happens inside the
-// solve.  The matrix does not change during a solve, so after deciding to
-// continue, the producer lane already issues the first stages of the next
-// SpMV, and their loads overlap the P phase and the barrier.
+// solve.  The matrix does not change during a solve, so once the P phase
+// has decided to go on, the producer lane already issues the first stages
+// of the next SpMV; their loads overlap the rest of the P phase and the
+// barrier.
 //
 // Every wait (mbarrier, grid barrier) is bounded in time: on a timeout the
 // kernel records ST_WAIT_TIMEOUT, waits (bounded) for its own copies in
@@ -103,6 +104,8 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned l
   return *ok_sh != 0;
 }
 
+constexpr int kTileCache = 256;   // tiles per CTA whose block ranges stay in shared memory
+
 struct LoopArgs {
   PipeMatrix m;
   const float* b;          // float[n][3]
@@ -170,6 +173,11 @@ pcg_loop(LoopArgs a) {
   __shared__ int stop_sh;
   __shared__ float scal_sh;
   __shared__ Lead L;
+  // every SpMV pass walks the same tiles: their block ranges, once
+  __shared__ int2 tb_sh[kTileCache];
+  PipeMatrix m = a.m;
+  m.tb = tb_sh;
+  m.ntb = fill_tile_bounds(m, tb_sh, kTileCache);
   pipe_init(sh);
   __syncthreads();
 
@@ -182,7 +190,7 @@ pcg_loop(LoopArgs a) {
   const bool timer = a.phase_ns != nullptr && blockIdx.x == 0 && tid == 0;
   Consumer C;
   if (tid == 0) {
-    producer_begin(L.P, a.m);
+    producer_begin(L.P, m);
     L.epoch = L.t_s = L.t_u = L.t_p = L.n_timed = L.t_prev = 0;
   }
   consumer_begin(C);
@@ -241,7 +249,7 @@ pcg_loop(LoopArgs a) {
       if (!stop) {
         Producer P = L.P;
         for (int j = 0; j < kPipeStages && !P.ended; ++j)
-          if (producer_step<BW>(P, sh, a.m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
+          if (producer_step<BW>(P, sh, m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
         L.P = P;
       }
     }
@@ -256,7 +264,7 @@ pcg_loop(LoopArgs a) {
     if (tid < 32) {
       if (tid == 0) {
         Producer P = L.P;
-        if (!producer_pass<BW>(P, sh, a.m)) atomicOr(a.status, ST_WAIT_TIMEOUT);
+        if (!producer_pass<BW>(P, sh, m)) atomicOr(a.status, ST_WAIT_TIMEOUT);
         L.P = P;
       }
     } else {
@@ -302,21 +310,27 @@ pcg_loop(LoopArgs a) {
     }
     if (stop_sh) break;
     const float alpha = scal_sh;
-    const Vec vm = vec_access();
     {
       float arz = 0.f, arr = 0.f;
-      for (int32_t f = tid; f < nslots; f += kPipeThreads) {
-        const int32_t i = own_row(f);
-        if (i >= n) break;   // rows grow with f: the rest are past the end too
-        const float4 qv = vm.ld(a.q + i), rv = vm.ld(a.r + i);
-        const float4 pu = vm.ld(a.pinv8 + 2 * int64_t(i)), pw = vm.ld(a.pinv8 + 2 * int64_t(i) + 1);
-        const float3 rn = make_float3(fmaf(-alpha, qv.x, rv.x), fmaf(-alpha, qv.y, rv.y),
-                                      fmaf(-alpha, qv.z, rv.z));
-        const float3 zn = apply_p(pu, pw, rn);
-        vm.st(a.r + i, make_float4(rn.x, rn.y, rn.z, 0.f));
-        vm.st(a.z + i, make_float4(zn.x, zn.y, zn.z, 0.f));
-        arz += dot3(rn, zn);
-        arr += dot3(rn, rn);
+      {
+        const float4* __restrict__ qv_ = a.q;
+        const float4* __restrict__ pinv = a.pinv8;
+        float4* __restrict__ rv_ = a.r;
+        float4* __restrict__ zv_ = a.z;
+#pragma unroll 2
+        for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+          const int32_t i = own_row(f);
+          if (i >= n) break;   // rows grow with f: the rest are past the end too
+          const float4 qv = qv_[i], rv = rv_[i];
+          const float4 pu = pinv[2 * int64_t(i)], pw = pinv[2 * int64_t(i) + 1];
+          const float3 rn = make_float3(fmaf(-alpha, qv.x, rv.x), fmaf(-alpha, qv.y, rv.y),
+                                        fmaf(-alpha, qv.z, rv.z));
+          const float3 zn = apply_p(pu, pw, rn);
+          rv_[i] = make_float4(rn.x, rn.y, rn.z, 0.f);
+          zv_[i] = make_float4(zn.x, zn.y, zn.z, 0.f);
+          arz += dot3(rn, zn);
+          arr += dot3(rn, rn);
+        }
       }
       Dfloat o[2] = {df_of(arz), df_of(arr)};
       block_sum_df<kPipeThreads, 2>(o, red_sh);
@@ -361,11 +375,10 @@ pcg_loop(LoopArgs a) {
         stop_sh = stop;
         L.rr_last = rr;
         L.rz_old = rz;
-        // the next SpMV streams the same matrix: start its first stages now
         if (!stop) {
           Producer P = L.P;
           for (int j = 0; j < kPipeStages && !P.ended; ++j)
-            if (producer_step<BW>(P, sh, a.m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
+            if (producer_step<BW>(P, sh, m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
           L.P = P;
         }
       }
@@ -376,17 +389,20 @@ pcg_loop(LoopArgs a) {
     const bool stop = stop_sh != 0;
     {
       const float beta = scal_sh;
+      float4* __restrict__ pv_ = a.p;
+      float4* __restrict__ dv_ = a.dv;
+      const float4* __restrict__ zv_ = a.z;
+#pragma unroll 2
       for (int32_t f = tid; f < nslots; f += kPipeThreads) {
         const int32_t i = own_row(f);
         if (i >= n) break;
-        const float4 pv = vm.ld(a.p + i), dvv = vm.ld(a.dv + i);
-        vm.st(a.dv + i, make_float4(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
-                                    fmaf(alpha, pv.z, dvv.z), 0.f));
-        if (!stop) {
-          const float4 zv = vm.ld(a.z + i);
-          vm.st(a.p + i, make_float4(fmaf(beta, pv.x, zv.x), fmaf(beta, pv.y, zv.y),
-                                     fmaf(beta, pv.z, zv.z), 0.f));
-        }
+        const float4 pv = pv_[i], dvv = dv_[i];
+        const float4 zv = stop ? pv : zv_[i];
+        dv_[i] = make_float4(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
+                             fmaf(alpha, pv.z, dvv.z), 0.f);
+        if (!stop)
+          pv_[i] = make_float4(fmaf(beta, pv.x, zv.x), fmaf(beta, pv.y, zv.y),
+                               fmaf(beta, pv.z, zv.z), 0.f);
       }
     }
     if (stop) break;
@@ -493,7 +509,8 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
   cudaStream_t s = h->stream;
   const bool prof = h->prof.on;
   LoopArgs a{};
-  a.m = PipeMatrix{h->n, (h->n + kPipeRows - 1) / kPipeRows, h->rowptr, h->colind, h->vals};
+  a.m = PipeMatrix{h->n, (h->n + kPipeRows - 1) / kPipeRows, h->rowptr, h->colind, h->vals,
+                   nullptr, 0};
   a.b = h->rhs;
   a.pinv8 = h->pinv8;
   a.dv = h->dv4;
@@ -642,7 +659,7 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
   float2* rec = reinterpret_cast<float2*>(v4 + 8 * kStaticVec);
   unsigned char* tail = reinterpret_cast<unsigned char*>(rec + size_t(kRecSlots) * kStaticMaxRecords);
   LoopArgs a{};
-  a.m = PipeMatrix{n, (n + kPipeRows - 1) / kPipeRows, rowptr, colind, vals};
+  a.m = PipeMatrix{n, (n + kPipeRows - 1) / kPipeRows, rowptr, colind, vals, nullptr, 0};
   a.b = b;
   float4* pinv8 = v4;
   a.pinv8 = pinv8;

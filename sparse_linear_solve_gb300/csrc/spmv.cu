@@ -85,7 +85,8 @@ int launch_spmv(Handle* h, const float* in, float* out) {
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(spmv)");
     if (h->device >= 0 && h->device < 64) g_attr_done[h->device] = true;
   }
-  PipeMatrix m{h->n, (h->n + kPipeRows - 1) / kPipeRows, h->rowptr, h->colind, h->vals};
+  PipeMatrix m{h->n, (h->n + kPipeRows - 1) / kPipeRows, h->rowptr, h->colind, h->vals,
+               nullptr, 0};
   spmv_plain<kSymBlock><<<h->spmv_grid, kPipeThreads, smem, h->stream>>>(m, in, out,
                                                                         h->d_status);
   h->launches += 1;

@@ -126,12 +126,16 @@ __device__ __forceinline__ float4 block_times(const float* __restrict__ B, float
                      fmaf(B[6], x.x, fmaf(B[7], x.y, B[8] * x.z)), 0.f);
 }
 
-// The matrix a pass streams.
+// The matrix a pass streams.  tb, if set, is a shared-memory copy of the
+// block ranges of this CTA's first ntb tiles (entry j: tile blockIdx.x +
+// j * gridDim.x), for kernels that walk the same tiles many times.
 struct PipeMatrix {
   int32_t n, ntiles;
   const int32_t* rowptr;
   const int32_t* colind;
   const float* vals;
+  const int2* tb;
+  int32_t ntb;
 };
 
 struct PipeShared {
@@ -182,17 +186,39 @@ struct Producer {
   uint64_t pol;
 };
 
-// Block range [rowptr[r0], rowptr[r0 + rows]) of a tile; loads issued here
-// are consumed a stage or more later, so their latency is off the path.
+// Block range [rowptr[r0], rowptr[r0 + rows]) of a tile: from the shared
+// copy when there is one, else loaded here and consumed a stage or more
+// later, so that the load's latency is off the producer's path.
 __device__ __forceinline__ void tile_bounds_of(const PipeMatrix& m, int32_t tile, int32_t& b0,
                                                int32_t& b1) {
   if (tile < m.ntiles) {
-    const int32_t r0 = tile * kPipeRows;
-    b0 = m.rowptr[r0];
-    b1 = m.rowptr[min(r0 + kPipeRows, m.n)];
+    const int32_t j = (tile - int32_t(blockIdx.x)) / int32_t(gridDim.x);
+    if (m.tb != nullptr && j < m.ntb) {
+      const int2 t = m.tb[j];
+      b0 = t.x;
+      b1 = t.y;
+    } else {
+      const int32_t r0 = tile * kPipeRows;
+      b0 = m.rowptr[r0];
+      b1 = m.rowptr[min(r0 + kPipeRows, m.n)];
+    }
   } else {
     b0 = b1 = 0;
   }
+}
+
+// Fills a shared copy of the block ranges of this CTA's first `cap` tiles
+// (all threads of the CTA; the caller synchronises afterwards).  Returns the
+// number of entries.
+__device__ __forceinline__ int32_t fill_tile_bounds(const PipeMatrix& m, int2* tb, int32_t cap) {
+  const int32_t mine = (m.ntiles - int32_t(blockIdx.x) + int32_t(gridDim.x) - 1) /
+                       int32_t(gridDim.x);
+  const int32_t cnt = mine < cap ? mine : cap;
+  for (int32_t j = threadIdx.x; j < cnt; j += blockDim.x) {
+    const int32_t r0 = (int32_t(blockIdx.x) + j * int32_t(gridDim.x)) * kPipeRows;
+    tb[j] = make_int2(m.rowptr[r0], m.rowptr[min(r0 + kPipeRows, m.n)]);
+  }
+  return cnt;
 }
 static_assert(kPipeStages <= 32, "slot bit masks");
 
