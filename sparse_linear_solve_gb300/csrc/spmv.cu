@@ -31,12 +31,17 @@ struct PlainEpi {
   }
 };
 
+constexpr int kTileCacheSpmv = 256;   // tiles per CTA whose block ranges go to shared memory
+
 template <int BW>
 __global__ void __launch_bounds__(kPipeThreads)
 spmv_plain(PipeMatrix m, const float* __restrict__ in, float* __restrict__ out,
            uint32_t* status) {
   extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int2 tb_sh[kTileCacheSpmv];
   const PipeShared sh = pipe_shared<BW>(smem);
+  m.tb = tb_sh;
+  m.ntb = fill_tile_bounds(m, tb_sh, kTileCacheSpmv);
   pipe_init(sh);
   __syncthreads();
   if (threadIdx.x < 32) {
