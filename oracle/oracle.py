@@ -50,6 +50,10 @@ def lib():
                                  ctypes.POINTER(ctypes.c_int32),
                                  ctypes.POINTER(ctypes.c_double)]
         L.oracle_pcg.restype = ctypes.c_int
+        L.oracle_pcg_x0.argtypes = [ctypes.c_void_p, ctypes.c_double, ctypes.c_int32, _f64p,
+                                    _f64p, ctypes.POINTER(ctypes.c_int32),
+                                    ctypes.POINTER(ctypes.c_double)]
+        L.oracle_pcg_x0.restype = ctypes.c_int
         L.oracle_update.argtypes = [ctypes.c_int32, _f32p, _f32p, _f64p, ctypes.c_double,
                                     _f64p, _f64p]
         L.oracle_update.restype = None
@@ -105,13 +109,23 @@ class System:
         lib().oracle_spmv(self._handle, xin, y)
         return y.reshape(self.n, 3)
 
-    def pcg(self, tol: float, maxit: int):
-        """Block-Jacobi PCG on A dv = b (Eq. (3) text): (dv, iterations, relres, status)."""
+    def pcg(self, tol: float, maxit: int, x0=None):
+        """Block-Jacobi PCG on A dv = b (Eq. (3) text): (dv, iterations, relres, status).
+
+        x0: optional initial guess (n x 3); the residual then starts as
+        b - A x0 and a guess that already meets |r| <= tol |b| is returned
+        after 0 iterations."""
         dv = np.zeros(self.n * 3, np.float64)
         it = ctypes.c_int32(0)
         rr = ctypes.c_double(0.0)
-        st = lib().oracle_pcg(self._handle, float(tol), int(maxit), dv,
-                              ctypes.byref(it), ctypes.byref(rr))
+        if x0 is None:
+            st = lib().oracle_pcg(self._handle, float(tol), int(maxit), dv,
+                                  ctypes.byref(it), ctypes.byref(rr))
+        else:
+            g = _c(x0, np.float64).reshape(-1)
+            assert g.shape[0] == self.n * 3
+            st = lib().oracle_pcg_x0(self._handle, float(tol), int(maxit), g, dv,
+                                     ctypes.byref(it), ctypes.byref(rr))
         return dv.reshape(self.n, 3), int(it.value), float(rr.value), int(st)
 
     def dense(self) -> np.ndarray:

@@ -266,8 +266,12 @@ void apply_pinv(const System& s, const std::vector<double>& r,
 
 // Textbook preconditioned CG on A dv = b, dv_0 = 0, stop when the recursive
 // residual satisfies |r|_2 <= tol |b|_2 (checked after each update of r).
+// PCG from the initial guess x0 (nullptr: dv = 0).  With a guess the
+// residual starts as r = b - A x0 and the iteration is otherwise unchanged;
+// the stop test stays |r| <= tol |b|, and a guess that already meets it is
+// returned after 0 iterations.
 int pcg(const System& s, double tol, int32_t maxit, double* dv_out,
-        int32_t* iters, double* relres) {
+        int32_t* iters, double* relres, const double* x0 = nullptr) {
   const size_t m = size_t(s.n) * 3;
   std::vector<double> dv(m, 0.0), r(s.rhs), z(m), p(m), q(m);
   *iters = 0;
@@ -277,10 +281,22 @@ int pcg(const System& s, double tol, int32_t maxit, double* dv_out,
     *relres = 0.0;
     return OR_OK;
   }
+  if (x0 != nullptr) {
+    std::copy(x0, x0 + m, dv.begin());
+    spmv(s, dv.data(), q.data());
+    for (size_t t = 0; t < m; ++t) r[t] = s.rhs[t] - q[t];
+  }
+  double rnorm = std::sqrt(dot(r, r));
+  if (x0 != nullptr) {
+    *relres = rnorm / bnorm;
+    if (rnorm <= tol * bnorm || maxit <= 0) {
+      std::copy(dv.begin(), dv.end(), dv_out);
+      return rnorm <= tol * bnorm ? OR_OK : OR_NOT_CONVERGED;
+    }
+  }
   apply_pinv(s, r, z);
   p = z;
   double rz = dot(r, z);
-  double rnorm = bnorm;
   for (int32_t it = 1; it <= maxit; ++it) {
     spmv(s, p.data(), q.data());
     double pq = dot(p, q);
@@ -375,6 +391,12 @@ void oracle_spmv(const void* sys, const double* xin, double* y) {
 int oracle_pcg(const void* sys, double tol, int32_t maxit, double* dv,
                int32_t* iters, double* relres) {
   return pcg(*static_cast<const System*>(sys), tol, maxit, dv, iters, relres);
+}
+
+// The same PCG started from the guess x0 (float64[n][3]).
+int oracle_pcg_x0(const void* sys, double tol, int32_t maxit, const double* x0, double* dv,
+                  int32_t* iters, double* relres) {
+  return pcg(*static_cast<const System*>(sys), tol, maxit, dv, iters, relres, x0);
 }
 
 // Backward-Euler state update of Eq. (3): v <- v + dv, then x <- x + h v.

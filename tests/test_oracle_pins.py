@@ -280,3 +280,53 @@ def test_spmv_against_dense():
     x = np.random.default_rng(3).normal(size=(w.n_verts, 3))
     np.testing.assert_allclose(s.spmv(x).reshape(-1), s.dense() @ x.reshape(-1),
                                rtol=1e-13, atol=1e-13)
+
+
+# ---- PCG from an initial guess (warm start) -----------------------------
+
+def _solution_lu(s):
+    return np.linalg.solve(s.dense(), s.b.reshape(-1)).reshape(-1, 3)
+
+
+def test_guess_at_the_solution_takes_no_iteration():
+    w = _tiny(8, rest_from_grid=True)
+    s = oracle.assemble_workload(w, w.x0, w.v0)
+    x = _solution_lu(s)
+    dv, it, rr, st = s.pcg(1e-8, 100, x0=x)
+    assert st == oracle.OK and it == 0
+    np.testing.assert_array_equal(dv, x)
+    # both residuals are rounding noise of an exact solution
+    true = np.linalg.norm(s.b.reshape(-1) - s.dense() @ x.reshape(-1)) / np.linalg.norm(s.b)
+    assert rr <= 1e-13 and true <= 1e-13
+
+
+def test_guess_with_no_iteration_reports_its_own_residual():
+    """maxit = 0: the returned residual is |b - A x0| / |b| (numpy, dense)."""
+    w = _tiny(8, rest_from_grid=True)
+    s = oracle.assemble_workload(w, w.x0, w.v0)
+    x0 = np.random.default_rng(5).normal(size=(w.n_verts, 3)) * 1e-3
+    dv, it, rr, st = s.pcg(1e-8, 0, x0=x0)
+    assert st == oracle.NOT_CONVERGED and it == 0
+    np.testing.assert_array_equal(dv, x0)
+    true = np.linalg.norm(s.b.reshape(-1) - s.dense() @ x0.reshape(-1)) / np.linalg.norm(s.b)
+    assert rr == pytest.approx(true, rel=1e-12)
+
+
+def test_any_guess_converges_to_the_dense_solution():
+    w = _tiny(8, rest_from_grid=True)
+    s = oracle.assemble_workload(w, w.x0, w.v0)
+    x = _solution_lu(s)
+    x0 = np.random.default_rng(6).normal(size=x.shape) * np.abs(x).max()
+    dv, it, rr, st = s.pcg(1e-12, 10000, x0=x0)
+    assert st == oracle.OK and rr <= 1e-12 and it > 0
+    assert np.linalg.norm(dv - x) <= 1e-10 * np.linalg.norm(x)
+
+
+def test_zero_guess_is_the_cold_start_bit_for_bit():
+    """b - A 0 = b exactly, so a zero guess must follow the cold iteration."""
+    w = _tiny(16, rest_from_grid=True)
+    s = oracle.assemble_workload(w, w.x0, w.v0)
+    cold = s.pcg(1e-8, 10000)
+    warm = s.pcg(1e-8, 10000, x0=np.zeros((w.n_verts, 3)))
+    np.testing.assert_array_equal(cold[0], warm[0])
+    assert cold[1:] == warm[1:]
