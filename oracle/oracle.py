@@ -57,6 +57,9 @@ def lib():
         L.oracle_update.argtypes = [ctypes.c_int32, _f32p, _f32p, _f64p, ctypes.c_double,
                                     _f64p, _f64p]
         L.oracle_update.restype = None
+        L.oracle_find_contacts.argtypes = [ctypes.c_int32, _f32p, ctypes.c_float, ctypes.c_int32,
+                                           _i32p, _i32p, _i32p, _i32p, ctypes.c_int64]
+        L.oracle_find_contacts.restype = ctypes.c_int64
         L.oracle_free.argtypes = [ctypes.c_void_p]
         L.oracle_free.restype = None
         _LIB = L
@@ -183,6 +186,25 @@ def assemble_workload(w, x, v, contacts=None) -> System:
         c = (contacts.i, contacts.j, contacts.k, contacts.rest)
     return assemble(w.n_verts, w.mass, w.gravity,
                     (w.spring_i, w.spring_j, w.spring_k, w.spring_rest), c, x, v, w.h)
+
+
+def find_contacts(x, radius, springs, capacity=None):
+    """Vertex pairs i < j closer than `radius` that are not springs, in (i, j)
+    order (P-Cloth Sec. 4.2-4.3, vertex-vertex proximity), by brute force
+    over all pairs with the distance test in float32 (the GPU's precision).
+    Returns (i, j, total); i and j hold min(total, capacity) pairs."""
+    x = _c(x, np.float32).reshape(-1, 3)
+    n = x.shape[0]
+    si = _c(springs[0], np.int32)
+    sj = _c(springs[1], np.int32)
+    cap = n * (n - 1) // 2 if capacity is None else int(capacity)
+    cap = max(cap, 1)
+    oi = np.zeros(cap, np.int32)
+    oj = np.zeros(cap, np.int32)
+    total = int(lib().oracle_find_contacts(n, x.reshape(-1), float(radius), si.shape[0], si, sj,
+                                           oi, oj, cap))
+    k = min(total, cap)
+    return oi[:k], oj[:k], total
 
 
 def update(x, v, dv, h):

@@ -30,6 +30,13 @@
 //   Sec. 3.1 / Eq. (3) text: the system is solved by preconditioned conjugate
 //     gradients; the page does not name the preconditioner, this oracle uses
 //     the inverse of each 3x3 diagonal block (block Jacobi).
+//   Sec. 4.2-4.3 (proximity contacts, restricted to vertex pairs): every pair
+//     of vertices i < j closer than a radius r that is not a spring becomes a
+//     contact (a spring of stiffness k_c and rest length r), listed in (i, j)
+//     order.  This is a brute-force test of all pairs.  The distance decides
+//     an integer outcome, so it is taken in the GPU's precision: float32
+//     differences, squared distance ((dx dx + dy dy) + dz dz) rounded after
+//     every operation, compared strictly with r r rounded to float32.
 //
 // Everything is double precision and single threaded.  The only library
 // primitives used are std::sort / std::unique / std::lower_bound and sqrt.
@@ -409,5 +416,39 @@ void oracle_update(int32_t n, const float* x, const float* v, const double* dv,
 }
 
 void oracle_free(void* sys) { delete static_cast<System*>(sys); }
+
+// Vertex-vertex proximity contacts (see the header): writes up to `capacity`
+// pairs (i, j), i < j, in (i, j) order and returns how many exist.  Spring
+// pairs (si[s], sj[s]), in either order, are not contacts.
+int64_t oracle_find_contacts(int32_t n, const float* x, float radius, int32_t ns,
+                             const int32_t* si, const int32_t* sj, int32_t* out_i,
+                             int32_t* out_j, int64_t capacity) {
+  std::vector<std::pair<int32_t, int32_t>> springs;
+  springs.reserve(size_t(ns));
+  for (int32_t s = 0; s < ns; ++s)
+    springs.emplace_back(std::min(si[s], sj[s]), std::max(si[s], sj[s]));
+  std::sort(springs.begin(), springs.end());
+  const float r2 = radius * radius;
+  int64_t count = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    for (int32_t j = i + 1; j < n; ++j) {
+      const float dx = x[3 * size_t(j)] - x[3 * size_t(i)];
+      const float dy = x[3 * size_t(j) + 1] - x[3 * size_t(i) + 1];
+      const float dz = x[3 * size_t(j) + 2] - x[3 * size_t(i) + 2];
+      const float xx = dx * dx;
+      const float yy = dy * dy;
+      const float zz = dz * dz;
+      const float d2 = (xx + yy) + zz;
+      if (!(d2 < r2)) continue;
+      if (std::binary_search(springs.begin(), springs.end(), std::make_pair(i, j))) continue;
+      if (count < capacity) {
+        out_i[count] = i;
+        out_j[count] = j;
+      }
+      ++count;
+    }
+  }
+  return count;
+}
 
 }  // extern "C"

@@ -330,3 +330,59 @@ def test_zero_guess_is_the_cold_start_bit_for_bit():
     warm = s.pcg(1e-8, 10000, x0=np.zeros((w.n_verts, 3)))
     np.testing.assert_array_equal(cold[0], warm[0])
     assert cold[1:] == warm[1:]
+
+
+# ---- vertex-vertex proximity contacts ------------------------------------
+
+def _numpy_pairs(x, radius, springs):
+    """Independent restatement: all pairs in float32 numpy arithmetic."""
+    x = np.asarray(x, np.float32)
+    n = x.shape[0]
+    excl = {(min(a, b), max(a, b)) for a, b in zip(springs[0], springs[1])}
+    r2 = np.float32(radius) * np.float32(radius)
+    out = []
+    for i in range(n):
+        d = x[i + 1:] - x[i]
+        d2 = (d[:, 0] * d[:, 0] + d[:, 1] * d[:, 1]) + d[:, 2] * d[:, 2]
+        for j in (np.nonzero(d2 < r2)[0] + i + 1):
+            if (i, int(j)) not in excl:
+                out.append((i, int(j)))
+    return out
+
+
+def test_contacts_hand_case():
+    # A-B 1.5 mm, B-D 1.9 mm, A-C 2.1 mm, A-D sqrt(1.5^2 + 1.9^2) = 2.42 mm
+    x = np.array([[0, 0, 0], [0.0015, 0, 0], [0, 0.0021, 0], [0.0015, 0, 0.0019]], np.float32)
+    none = (np.zeros(0, np.int32), np.zeros(0, np.int32))
+    i, j, total = oracle.find_contacts(x, 2e-3, none)
+    assert total == 2 and list(zip(i, j)) == [(0, 1), (1, 3)]
+    # a spring between A and B (given as B-A) removes that pair
+    i, j, total = oracle.find_contacts(x, 2e-3, (np.array([1], np.int32), np.array([0], np.int32)))
+    assert total == 1 and list(zip(i, j)) == [(1, 3)]
+
+
+def test_contacts_radius_is_strict():
+    r = 0.25   # r and r^2 exact in float32
+    none = (np.zeros(0, np.int32), np.zeros(0, np.int32))
+    at = np.array([[0, 0, 0], [r, 0, 0]], np.float32)
+    assert oracle.find_contacts(at, r, none)[2] == 0
+    inside = np.array([[0, 0, 0], [np.nextafter(np.float32(r), np.float32(0)), 0, 0]], np.float32)
+    assert oracle.find_contacts(inside, r, none)[2] == 1
+
+
+def test_contacts_match_a_numpy_float32_restatement():
+    rng = np.random.default_rng(21)
+    x = rng.uniform(0, 0.03, size=(400, 3)).astype(np.float32)
+    springs = (rng.integers(0, 400, 300).astype(np.int32), rng.integers(0, 400, 300).astype(np.int32))
+    i, j, total = oracle.find_contacts(x, 4e-3, springs)
+    ref = _numpy_pairs(x, 4e-3, springs)
+    assert total == len(ref) > 50
+    assert list(zip(i.tolist(), j.tolist())) == ref
+
+
+def test_contacts_beyond_capacity_are_counted():
+    x = np.zeros((10, 3), np.float32)   # every pair at distance 0
+    none = (np.zeros(0, np.int32), np.zeros(0, np.int32))
+    i, j, total = oracle.find_contacts(x, 1e-3, none, capacity=7)
+    assert total == 45 and len(i) == 7
+    assert list(zip(i, j)) == [(0, 1), (0, 2), (0, 3), (0, 4), (0, 5), (0, 6), (0, 7)]
