@@ -45,6 +45,7 @@ def parse():
     p.add_argument("--config", default="C5", help="workload C1..C5 (default C5)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-layouts", action="store_true", help="skip the SpMV layout comparison")
     p.add_argument("--oracle-iters", type=int, default=8,
                    help="oracle PCG iterations per reference sample step")
     return p.parse_args()
@@ -187,6 +188,44 @@ def max_over_ranks(x, device):
 def whole_job_rate(world, units_per_rank, seconds):
     """Units all ranks processed per second of the slowest rank."""
     return world * units_per_rank / seconds
+
+
+# ------------------------------------------------------- SpMV layouts --
+def spmv_layouts(cloth, n, dev, reps=50):
+    """The plain product out = A in of the last assembled matrix in the two
+    layouts: streamed BSR3 (pcloth_spmv) and the pages' block-ELL tables
+    (pcloth_spmv_bell), each timed over `reps` launches with CUDA events (A
+    is larger than L2, so every launch streams it from HBM)."""
+    import torch
+    x = torch.randn(n, 3, device=dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(5):
+            fn(x, y)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn(x, y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3   # us per launch
+
+    nnzb = cloth.nnzb()
+    algo = 28 * nnzb + 28 * n
+    bsr_us = timed(cloth.spmv)
+    width = cloth.bell_build()
+    bell_us = timed(cloth.spmv_bell)
+    peak, _ = hbm_peak()
+    return dict(bytes_per_launch=algo,
+                bsr3=dict(us=bsr_us, gbs=algo / (bsr_us * 1e-6) / 1e9,
+                          frac=algo / (bsr_us * 1e-6) / 1e9 / peak),
+                block_ell=dict(us=bell_us, gbs=algo / (bell_us * 1e-6) / 1e9,
+                               frac=algo / (bell_us * 1e-6) / 1e9 / peak, width=width,
+                               table_slots_per_block=width * n / nnzb),
+                timing="CUDA events over %d launches each, same matrix and input" % reps)
 
 
 # ------------------------------------------------------------------- arms --
@@ -340,6 +379,8 @@ def run_ours(args, rank, world, local_rank):
         gpu_launches=int(prof_clean["kernel_launches"]),
         e2e=e2e,
     )
+    if not args.no_layouts:
+        result["spmv_layouts"] = spmv_layouts(cloth, n, dev)
 
     # ---- CPU baseline: the oracle on the host cores, bounded sample ------
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -124,6 +124,22 @@ int pcloth_assemble(pcloth_t h, const float* x, const float* v,
  * out must not overlap).  Sec. 3.1 (SpMV).  Asynchronous. */
 int pcloth_spmv(pcloth_t h, const float* in, float* out);
 
+/* Block-ELL comparison path (P-Cloth Sec. 3.2.2: the pages' index and value
+ * tables, padded to the longest compacted row, read by one thread per row).
+ * pcloth_bell_build copies the last assembled matrix into that layout:
+ * W = the longest row in blocks, slot s of row i at s * n + i, column
+ * indices int32[W * n] (-1 past a row's end) and six planes of the packed
+ * symmetric block values float32[6][W * n].  It writes W to *width (may be
+ * NULL) and synchronises.  It is the one call after create that may
+ * allocate device memory (the tables grow to the largest W * n seen, and are
+ * freed by pcloth_destroy).  The copy is invalid after the next assembly.
+ * pcloth_spmv_bell computes out = A in (device float32[n][3] each) from the
+ * copy, adding the same products in the same order as pcloth_spmv, so the
+ * two give the same bits; PCLOTH_ERR_STATE if there is no valid copy.
+ * Asynchronous. */
+int pcloth_bell_build(pcloth_t h, int32_t* width);
+int pcloth_spmv_bell(pcloth_t h, const float* in, float* out);
+
 /* Solve A dv = b by block-Jacobi PCG from dv = 0 until
  * |r|_2 <= tol |b|_2 (recursive residual) or maxit iterations; dv is device
  * float32[n][3]; *iterations and *rel_residual (= |r|/|b|) are written on

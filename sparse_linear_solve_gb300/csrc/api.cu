@@ -39,7 +39,7 @@ void free_handle(Handle* h) {
                   h->newfirst, h->tile_nb, h->tile_eb, h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
                   h->dv, h->dv4, h->r4, h->z4, h->p4, h->q4, h->rec, h->bar,
-                  h->phase_ns, h->state, h->d_status};
+                  h->phase_ns, h->state, h->d_status, h->bell_wmax, h->bell_col, h->bell_val};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (h->state_host) cudaFreeHost(h->state_host);
@@ -253,6 +253,7 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->rec, int64_t(h->loop_grid) * kRecSlots));
   A(dalloc(&h->bar, 1));
   A(dalloc(&h->phase_ns, 4));
+  A(dalloc(&h->bell_wmax, 1));
   A(dalloc(&h->state, 1));
   A(dalloc(&h->d_status, 1));
   A(cudaMallocHost(reinterpret_cast<void**>(&h->state_host), sizeof(PcgState)));
@@ -320,6 +321,26 @@ int pcloth_spmv(pcloth_t ht, const float* in, float* out) {
   if (!h->assembled) return fail(h, PCLOTH_ERR_STATE, "spmv before assemble");
   cudaSetDevice(h->device);
   return launch_spmv(h, in, out);
+}
+
+int pcloth_bell_build(pcloth_t ht, int32_t* width) {
+  Handle* h = reinterpret_cast<Handle*>(ht);
+  if (!h) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "NULL handle");
+  if (!h->assembled) return fail(h, PCLOTH_ERR_STATE, "block-ELL copy before assemble");
+  cudaSetDevice(h->device);
+  const int rc = bell_build(h);
+  if (rc == PCLOTH_OK && width) *width = h->bell_w;
+  return rc;
+}
+
+int pcloth_spmv_bell(pcloth_t ht, const float* in, float* out) {
+  Handle* h = reinterpret_cast<Handle*>(ht);
+  if (!h) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "NULL handle");
+  if (!in || !out) return fail(h, PCLOTH_ERR_INVALID_ARG, "NULL vector");
+  if (!h->bell_valid)
+    return fail(h, PCLOTH_ERR_STATE, "no block-ELL copy of the current matrix (pcloth_bell_build)");
+  cudaSetDevice(h->device);
+  return launch_bell_spmv(h, in, out);
 }
 
 int pcloth_solve(pcloth_t ht, double tol, int32_t maxit, float* dv,

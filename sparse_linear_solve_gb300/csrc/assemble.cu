@@ -560,6 +560,7 @@ int assemble_system(Handle* h, const float* x, const float* v,
   const int B = h->key_bits;
   const int32_t ntiles = (h->n + kAsmRows - 1) / kAsmRows;
   cudaStream_t s = h->stream;
+  h->bell_valid = false;   // the pattern changes below
   if (h->prof.on) cudaEventRecord(h->ev[0], s);
   int rc = PCLOTH_OK;
   AsmArgs a{};

@@ -144,6 +144,15 @@ struct Handle {
   uint32_t* d_status = nullptr;    // device error bits
   uint32_t* h_status = nullptr;    // pinned copy
 
+  // block-ELL copy of the assembled matrix (the pages' layout), built on
+  // request for the head-to-head SpMV; invalid after the next assembly
+  int32_t* bell_wmax = nullptr;    // device: longest row
+  int32_t* bell_col = nullptr;     // [W * n]
+  float* bell_val = nullptr;       // [6][W * n]
+  int64_t bell_cap = 0;            // slots allocated
+  int32_t bell_w = 0;
+  bool bell_valid = false;
+
   // profiling
   Profile prof;
   cudaEvent_t ev[8] = {};
@@ -171,6 +180,10 @@ int assemble_system(Handle* h, const float* x, const float* v,
 int spmv_grid_for(int32_t n, int sm_count);
 int pipe_carveout_percent(size_t smem);
 int launch_spmv(Handle* h, const float* in, float* out);
+
+// bell.cu: block-ELL copy of the assembled matrix and its product
+int bell_build(Handle* h);
+int launch_bell_spmv(Handle* h, const float* in, float* out);
 
 // assemble.cu: expand the packed symmetric inverses to float[n][3][3]
 int launch_pinv_expand(Handle* h, float* out9);

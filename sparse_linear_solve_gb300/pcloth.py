@@ -30,7 +30,8 @@ CODE_NAMES = {OK: "OK", NOT_CONVERGED: "NOT_CONVERGED", ERR_INVALID_ARG: "INVALI
 EXPORTS = ("pcloth_create", "pcloth_assemble", "pcloth_spmv", "pcloth_solve", "pcloth_step",
            "pcloth_step_host", "pcloth_nnzb", "pcloth_export", "pcloth_set_stream",
            "pcloth_sync", "pcloth_last_error", "pcloth_destroy", "pcloth_profile_enable",
-           "pcloth_profile_read", "pcloth_solve_bsr3_static")
+           "pcloth_profile_read", "pcloth_solve_bsr3_static", "pcloth_bell_build",
+           "pcloth_spmv_bell")
 
 STATIC_MAX_VERTS = 16384   # PCLOTH_STATIC_MAX_VERTS
 
@@ -74,6 +75,8 @@ def lib():
         L.pcloth_create.argtypes = [P(Mesh), P(Springs), P(Opts), P(vp)]
         L.pcloth_assemble.argtypes = [vp, vp, vp, P(Springs), ctypes.c_float]
         L.pcloth_spmv.argtypes = [vp, vp, vp]
+        L.pcloth_bell_build.argtypes = [vp, P(i32)]
+        L.pcloth_spmv_bell.argtypes = [vp, vp, vp]
         L.pcloth_solve.argtypes = [vp, dbl, i32, vp, P(i32), P(dbl)]
         L.pcloth_step.argtypes = [vp, vp, vp, P(Springs), ctypes.c_float, dbl, i32, vp,
                                   P(i32), P(dbl)]
@@ -174,6 +177,23 @@ def pcloth_spmv(h: int, inp: torch.Tensor, out: torch.Tensor):
     _check(inp, torch.float32, None, None, "in")
     _check(out, torch.float32, inp.device, tuple(inp.shape), "out")
     rc = lib().pcloth_spmv(h, _ptr(inp), _ptr(out))
+    if rc != OK:
+        _raise(h, rc)
+
+
+def pcloth_bell_build(h: int) -> int:
+    """Block-ELL copy of the last assembled matrix; returns its width W."""
+    w = ctypes.c_int32(0)
+    rc = lib().pcloth_bell_build(h, ctypes.byref(w))
+    if rc != OK:
+        _raise(h, rc)
+    return int(w.value)
+
+
+def pcloth_spmv_bell(h: int, inp: torch.Tensor, out: torch.Tensor):
+    _check(inp, torch.float32, None, None, "in")
+    _check(out, torch.float32, inp.device, tuple(inp.shape), "out")
+    rc = lib().pcloth_spmv_bell(h, _ptr(inp), _ptr(out))
     if rc != OK:
         _raise(h, rc)
 
@@ -354,6 +374,16 @@ class PCloth:
         if out is None:
             out = torch.empty_like(inp)
         pcloth_spmv(self.h, inp, out)
+        return out
+
+    def bell_build(self) -> int:
+        return pcloth_bell_build(self.h)
+
+    def spmv_bell(self, inp: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        _check(inp, torch.float32, self.device, (self.n, 3), "in")
+        if out is None:
+            out = torch.empty_like(inp)
+        pcloth_spmv_bell(self.h, inp, out)
         return out
 
     def solve(self, tol: float, maxit: int, dv: Optional[torch.Tensor] = None):

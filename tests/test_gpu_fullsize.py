@@ -12,6 +12,7 @@ compare dv with the oracle's PCG directly.
 """
 import numpy as np
 import pytest
+import torch
 
 from oracle import oracle
 from sparse_linear_solve_gb300 import pcloth as pc
@@ -33,7 +34,12 @@ def test_fullsize_pcg_against_oracle(name):
     c = w.contacts(0)
     pcl, ref, _, _ = compare_assembly(w, w.x0, w.v0, c if c.n else None)
     x = np.random.default_rng(4).normal(size=(w.n_verts, 3)).astype(np.float32)
-    assert rel_l2(pcl.spmv(to_dev(x)).cpu().numpy(), ref.spmv(x)) <= 1e-5
+    xd = to_dev(x)
+    y = pcl.spmv(xd)
+    assert rel_l2(y.cpu().numpy(), ref.spmv(x)) <= 1e-5
+    # the block-ELL layout of the pages gives the same bits at full size
+    pcl.bell_build()
+    assert torch.equal(pcl.spmv_bell(xd), y)
     dv, it, rr, code = pcl.solve(w.tol, w.maxit)
     assert code == pc.OK and rr <= w.tol
     dv_ref, it_ref, rr_ref, st = ref.pcg(w.tol, w.maxit)
@@ -48,7 +54,12 @@ def test_fullsize_assembly_spmv_and_residual(name):
     c = w.contacts(0)
     pcl, ref, _, _ = compare_assembly(w, w.x0, w.v0, c)
     x = np.random.default_rng(4).normal(size=(w.n_verts, 3)).astype(np.float32)
-    assert rel_l2(pcl.spmv(to_dev(x)).cpu().numpy(), ref.spmv(x)) <= 1e-5
+    xd = to_dev(x)
+    y = pcl.spmv(xd)
+    assert rel_l2(y.cpu().numpy(), ref.spmv(x)) <= 1e-5
+    # the block-ELL layout of the pages gives the same bits at full size
+    pcl.bell_build()
+    assert torch.equal(pcl.spmv_bell(xd), y)
     dv, it, rr, code = pcl.solve(w.tol, w.maxit)
     assert code == pc.OK and rr <= w.tol
     d = dv.cpu().numpy().astype(np.float64)

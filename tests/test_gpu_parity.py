@@ -288,3 +288,38 @@ def test_profiling_times_every_iteration_and_changes_nothing():
         assert p["iterations"] == it and p["samples"] == it, (mode, p, it)
         assert p["spmv_ms"] > 0 and p["update_ms"] > 0 and p["assemble_calls"] == 1
         assert p["solve_ms"] >= p["spmv_ms"]
+
+
+@pytest.mark.parametrize("name", ["droop37", "twolayer33", "folded4x29"])
+def test_block_ell_spmv_matches_oracle_and_bsr3(name):
+    """The pages' block-ELL layout (P-Cloth Sec. 3.2.2 tables) gives the same
+    product as the oracle (1e-5) and the same bits as the BSR3 kernel (same
+    products in the same order)."""
+    w = small_configs()[name]
+    c = w.contacts(0)
+    pcl, ref, _, _ = compare_assembly(w, w.x0, w.v0, c if c.n else None)
+    W = pcl.bell_build()
+    g = pcl.export()
+    lengths = np.diff(g["rowptr"].cpu().numpy())
+    assert W == int(lengths.max())
+    x = np.random.default_rng(12).normal(size=(w.n_verts, 3)).astype(np.float32)
+    xd = to_dev(x)
+    y_bell = pcl.spmv_bell(xd)
+    y_bsr = pcl.spmv(xd)
+    assert rel_l2(y_bell.cpu().numpy(), ref.spmv(x)) <= 1e-5
+    assert torch.equal(y_bell, y_bsr)
+
+
+def test_block_ell_copy_is_invalid_after_the_next_assembly():
+    w = W.jittered_cloth(n=40, steps=2)
+    pcl = make(w)
+    xd, vd = to_dev(w.x0), to_dev(w.v0)
+    pcl.assemble(xd, vd, w.contacts(0), w.h)
+    pcl.bell_build()
+    pcl.spmv_bell(xd)
+    pcl.assemble(xd, vd, w.contacts(1), w.h)
+    with pytest.raises(pc.PClothError) as ei:
+        pcl.spmv_bell(xd)
+    assert ei.value.code == pc.ERR_STATE
+    pcl.bell_build()
+    assert torch.equal(pcl.spmv_bell(xd), pcl.spmv(xd))
