@@ -34,6 +34,8 @@ sys.path.insert(0, ROOT)
 METRIC = "PCG iterations/s + implicit steps/s at 1.65M tris; SpMV GB/s vs HBM peak"
 UNIT = "implicit steps/s"
 FALLBACK_HBM_GBS = 6800.0
+# contact radius of the multi-layer cloths when contacts are found geometrically
+FOUND_RADIUS = {"C4": 3e-3, "C5": 2e-3}
 
 
 def parse():
@@ -46,6 +48,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-layouts", action="store_true", help="skip the SpMV layout comparison")
+    p.add_argument("--contacts", choices=("synthetic", "found"), default="synthetic",
+                   help="synthetic: the configuration's seeded contact lists; found: vertex "
+                        "pairs closer than the contact radius, found by spatial hashing on "
+                        "the GPU every step inside the timed region (multi-layer cloths)")
     p.add_argument("--oracle-iters", type=int, default=8,
                    help="oracle PCG iterations per reference sample step")
     return p.parse_args()
@@ -241,14 +247,33 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     w = W.make(args.config)
     K, Wm = args.steps, args.warmup
+    found_mode = args.contacts == "found"
+    if found_mode:
+        # the configuration's contact radius; room for a growing contact set
+        radius = FOUND_RADIUS.get(args.config)
+        if radius is None:
+            raise SystemExit("--contacts found is for the multi-layer cloths (C4, C5)")
+        w.max_contacts = 6 * w.n_verts
+        args.no_e2e = True
+        args.no_cpu_baseline = True
     cloth = pc.PCloth.from_workload(w, device=dev)
     x = torch.from_numpy(w.x0).to(dev)
     v = torch.from_numpy(w.v0).to(dev)
     dv = torch.empty_like(x)
     host_contacts = [w.contacts(t) for t in range(Wm + K)]
     dev_contacts = [pc.to_device_elements(c, dev) for c in host_contacts]
+    found_counts = []
+
+    def one_step(t):
+        if found_mode:
+            c, nf = cloth.find_contacts(x, radius, W.K_CONTACT)
+            found_counts.append(nf)
+        else:
+            c = dev_contacts[t]
+        return cloth.step(x, v, c, w.h, w.tol, w.maxit, dv)
+
     for t in range(Wm):
-        cloth.step(x, v, dev_contacts[t], w.h, w.tol, w.maxit, dv)
+        one_step(t)
     torch.cuda.synchronize()
     x_start, v_start = x.clone(), v.clone()
 
@@ -265,8 +290,9 @@ def run_ours(args, rank, world, local_rank):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         its, codes = [], []
+        del found_counts[:]
         for t in range(K):
-            it, rr, code = cloth.step(x, v, dev_contacts[Wm + t], w.h, w.tol, w.maxit, dv)
+            it, rr, code = one_step(Wm + t)
             its.append(it)
             codes.append(code)
         e1.record(stream)
@@ -379,6 +405,12 @@ def run_ours(args, rank, world, local_rank):
         gpu_launches=int(prof_clean["kernel_launches"]),
         e2e=e2e,
     )
+    if found_mode:
+        result["config"]["contacts"] = ("found every step by spatial hashing inside the timed "
+                                        "region: vertex pairs closer than %g m that are not "
+                                        "springs, k = %g" % (radius, W.K_CONTACT))
+        result["config"]["contacts_per_step"] = sum(found_counts) / max(len(found_counts), 1)
+        result["e2e_note"] = "not measured in this mode (the contacts are found on the device)"
     if not args.no_layouts:
         result["spmv_layouts"] = spmv_layouts(cloth, n, dev)
 

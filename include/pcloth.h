@@ -124,6 +124,25 @@ int pcloth_assemble(pcloth_t h, const float* x, const float* v,
  * out must not overlap).  Sec. 3.1 (SpMV).  Asynchronous. */
 int pcloth_spmv(pcloth_t h, const float* in, float* out);
 
+/* Vertex-vertex proximity contacts by spatial hashing (P-Cloth Sec. 4.2: a
+ * spatial-hash table built every step, then proximity tests; Sec. 4.3:
+ * proximities enter the implicit integrator as forces), restricted to pairs
+ * of vertices.  Every pair i < j of vertices at x (device float32[n][3])
+ * closer than `radius` that is not a spring becomes a contact: a spring
+ * (i, j, stiffness, rest = radius), the same element law as the springs.
+ * The distance test is taken in float32 with every operation rounded:
+ * ((dx dx + dy dy) + dz dz) < radius * radius, d = x_j - x_i.  The pairs are
+ * written in (i, j) order into the caller's device arrays out->i, out->j
+ * (int32), out->k, out->rest (float32) of length `capacity`; out->n is set
+ * to their number, which is ready to pass to pcloth_assemble / pcloth_step.
+ * *found (may be NULL) receives the number of pairs found.  If more than
+ * min(capacity, max_contacts) exist, nothing is written, out->n = 0 and
+ * PCLOTH_ERR_CAPACITY is returned.  Cells have edge radius * (1 + 2^-7),
+ * which finds every pair for coordinates within 2^15 cells of the origin.
+ * Synchronises. */
+int pcloth_find_contacts(pcloth_t h, const float* x, float radius, float stiffness,
+                         pcloth_springs* out, int32_t capacity, int32_t* found);
+
 /* Block-ELL comparison path (P-Cloth Sec. 3.2.2: the pages' index and value
  * tables, padded to the longest compacted row, read by one thread per row).
  * pcloth_bell_build copies the last assembled matrix into that layout:

@@ -39,7 +39,8 @@ void free_handle(Handle* h) {
                   h->newfirst, h->tile_nb, h->tile_eb, h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
                   h->dv, h->dv4, h->r4, h->z4, h->p4, h->q4, h->rec, h->bar,
-                  h->phase_ns, h->state, h->d_status, h->bell_wmax, h->bell_col, h->bell_val};
+                  h->phase_ns, h->state, h->d_status, h->bell_wmax, h->bell_col, h->bell_val,
+                  h->vkey[0], h->vkey[1], h->vid[0], h->vid[1]};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (h->state_host) cudaFreeHost(h->state_host);
@@ -200,7 +201,8 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
 
   // ---- device buffers ---------------------------------------------------
   const int64_t ent2 = std::max<int64_t>(2 * mc, 1);
-  const int64_t sort_tiles = (ent2 + kSortTile - 1) / kSortTile;
+  // the radix sort also orders the n vertices by cell for contact finding
+  const int64_t sort_tiles = (std::max<int64_t>(ent2, n) + kSortTile - 1) / kSortTile;
   const int64_t scan_tiles = (ent2 + kScanTile - 1) / kScanTile;
   const int64_t asm_tiles = (n + kAsmRows - 1) / kAsmRows;
   h->spmv_grid = spmv_grid_for(int32_t(n), h->sm_count);
@@ -229,6 +231,8 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   for (int b = 0; b < 2; ++b) {
     A(dalloc(&h->ckey[b], ent2));
     A(dalloc(&h->cval[b], ent2));
+    A(dalloc(&h->vkey[b], n));
+    A(dalloc(&h->vid[b], n));
   }
   A(dalloc(&h->sort_counts, sort_tiles * kSortRadix + 1));
   A(dalloc(&h->flags, ent2 + 1));
@@ -321,6 +325,21 @@ int pcloth_spmv(pcloth_t ht, const float* in, float* out) {
   if (!h->assembled) return fail(h, PCLOTH_ERR_STATE, "spmv before assemble");
   cudaSetDevice(h->device);
   return launch_spmv(h, in, out);
+}
+
+int pcloth_find_contacts(pcloth_t ht, const float* x, float radius, float stiffness,
+                         pcloth_springs* out, int32_t capacity, int32_t* found) {
+  Handle* h = reinterpret_cast<Handle*>(ht);
+  if (!h) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "NULL handle");
+  if (!x || !out) return fail(h, PCLOTH_ERR_INVALID_ARG, "NULL x or out");
+  if (!(radius > 0.f) || !std::isfinite(radius) || !(stiffness >= 0.f) ||
+      !std::isfinite(stiffness))
+    return fail(h, PCLOTH_ERR_INVALID_ARG, "radius must be > 0 and stiffness >= 0");
+  if (capacity < 0) return fail(h, PCLOTH_ERR_INVALID_ARG, "negative capacity");
+  if (capacity > 0 && (!out->i || !out->j || !out->k || !out->rest))
+    return fail(h, PCLOTH_ERR_INVALID_ARG, "NULL output array");
+  cudaSetDevice(h->device);
+  return find_contacts(h, x, radius, stiffness, out, capacity, found);
 }
 
 int pcloth_bell_build(pcloth_t ht, int32_t* width) {

@@ -144,6 +144,10 @@ struct Handle {
   uint32_t* d_status = nullptr;    // device error bits
   uint32_t* h_status = nullptr;    // pinned copy
 
+  // contact finding: vertices sorted by spatial-hash cell
+  uint64_t* vkey[2] = {nullptr, nullptr};   // n
+  int32_t* vid[2] = {nullptr, nullptr};     // n
+
   // block-ELL copy of the assembled matrix (the pages' layout), built on
   // request for the head-to-head SpMV; invalid after the next assembly
   int32_t* bell_wmax = nullptr;    // device: longest row
@@ -180,6 +184,10 @@ int assemble_system(Handle* h, const float* x, const float* v,
 int spmv_grid_for(int32_t n, int sm_count);
 int pipe_carveout_percent(size_t smem);
 int launch_spmv(Handle* h, const float* in, float* out);
+
+// contacts.cu: vertex-vertex proximity contacts by spatial hashing
+int find_contacts(Handle* h, const float* x, float radius, float stiffness,
+                  pcloth_springs* out, int32_t capacity, int32_t* found);
 
 // bell.cu: block-ELL copy of the assembled matrix and its product
 int bell_build(Handle* h);

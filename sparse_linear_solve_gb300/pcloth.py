@@ -31,7 +31,7 @@ EXPORTS = ("pcloth_create", "pcloth_assemble", "pcloth_spmv", "pcloth_solve", "p
            "pcloth_step_host", "pcloth_nnzb", "pcloth_export", "pcloth_set_stream",
            "pcloth_sync", "pcloth_last_error", "pcloth_destroy", "pcloth_profile_enable",
            "pcloth_profile_read", "pcloth_solve_bsr3_static", "pcloth_bell_build",
-           "pcloth_spmv_bell")
+           "pcloth_spmv_bell", "pcloth_find_contacts")
 
 STATIC_MAX_VERTS = 16384   # PCLOTH_STATIC_MAX_VERTS
 
@@ -76,6 +76,8 @@ def lib():
         L.pcloth_assemble.argtypes = [vp, vp, vp, P(Springs), ctypes.c_float]
         L.pcloth_spmv.argtypes = [vp, vp, vp]
         L.pcloth_bell_build.argtypes = [vp, P(i32)]
+        L.pcloth_find_contacts.argtypes = [vp, vp, ctypes.c_float, ctypes.c_float, P(Springs),
+                                           i32, P(i32)]
         L.pcloth_spmv_bell.argtypes = [vp, vp, vp]
         L.pcloth_solve.argtypes = [vp, dbl, i32, vp, P(i32), P(dbl)]
         L.pcloth_step.argtypes = [vp, vp, vp, P(Springs), ctypes.c_float, dbl, i32, vp,
@@ -179,6 +181,33 @@ def pcloth_spmv(h: int, inp: torch.Tensor, out: torch.Tensor):
     rc = lib().pcloth_spmv(h, _ptr(inp), _ptr(out))
     if rc != OK:
         _raise(h, rc)
+
+
+def pcloth_find_contacts(h: int, x: torch.Tensor, radius: float, stiffness: float,
+                         capacity: int):
+    """Vertex pairs closer than `radius` (not springs) as contact springs:
+    returns ((i, j, k, rest) device tensors of length n_found, n_found).
+    Raises PClothError (ERR_CAPACITY) if more than `capacity` exist; the
+    count found is in the exception's `found` attribute."""
+    _check(x, torch.float32, None, None, "x")
+    dev = x.device
+    cap = max(int(capacity), 0)
+    oi = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    oj = torch.empty_like(oi)
+    ok = torch.empty(max(cap, 1), dtype=torch.float32, device=dev)
+    orest = torch.empty_like(ok)
+    out = Springs(0, _ptr(oi), _ptr(oj), _ptr(ok), _ptr(orest))
+    found = ctypes.c_int32(0)
+    rc = lib().pcloth_find_contacts(h, _ptr(x), float(radius), float(stiffness), ctypes.byref(out),
+                                    cap, ctypes.byref(found))
+    if rc != OK:
+        try:
+            _raise(h, rc)
+        except PClothError as e:
+            e.found = int(found.value)
+            raise
+    m = int(out.n)
+    return (oi[:m], oj[:m], ok[:m], orest[:m]), int(found.value)
 
 
 def pcloth_bell_build(h: int) -> int:
@@ -346,6 +375,7 @@ class PCloth:
         self.mass = _dev_tensor(mass, torch.float32, device)
         self.n = int(self.mass.shape[0])
         self.springs = to_device_elements(springs, device)
+        self.max_contacts = int(max_contacts)
         self.h = pcloth_create(self.mass, gravity, self.springs, max_contacts, stream)
         self._contacts = None
 
@@ -375,6 +405,14 @@ class PCloth:
             out = torch.empty_like(inp)
         pcloth_spmv(self.h, inp, out)
         return out
+
+    def find_contacts(self, x: torch.Tensor, radius: float, stiffness: float,
+                      capacity: Optional[int] = None):
+        """((i, j, k, rest), n_found): the vertex pairs of x closer than radius
+        that are not springs, as contact springs (rest = radius)."""
+        _check(x, torch.float32, self.device, (self.n, 3), "x")
+        return pcloth_find_contacts(self.h, x, radius, stiffness,
+                                    self.max_contacts if capacity is None else capacity)
 
     def bell_build(self) -> int:
         return pcloth_bell_build(self.h)
