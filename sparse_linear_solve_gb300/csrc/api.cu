@@ -33,12 +33,12 @@ void free_handle(Handle* h) {
   cudaSetDevice(h->device);
   cudaStreamSynchronize(h->stream);
   void* bufs[] = {h->mass, h->rowptr_s, h->colind_s, h->sblk_ptr, h->sentry,
-                  h->rowptr, h->colind, h->vals, h->rhs, h->pinv8,
+                  h->rowptr, h->colind, h->vals, h->rhs, h->pinv6,
                   h->ckey[0], h->ckey[1], h->cval[0], h->cval[1],
                   h->sort_counts, h->flags, h->scan_tmp, h->newkey,
                   h->newfirst, h->tile_nb, h->tile_eb, h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
-                  h->dv, h->dv4, h->r4, h->z4, h->p4, h->q4, h->rec, h->bar,
+                  h->dv, h->dv3, h->r3, h->z3, h->p4, h->q3, h->rec, h->bar,
                   h->phase_ns, h->state, h->d_status, h->bell_wmax, h->bell_col, h->bell_val,
                   h->vkey[0], h->vkey[1], h->vid[0], h->vid[1]};
   for (void* b : bufs)
@@ -227,7 +227,9 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->colind, cap + vpad));
   A(dalloc(&h->vals, cap * kSymBlock + vpad));
   A(dalloc(&h->rhs, 3 * n + vpad));
-  A(dalloc(&h->pinv8, 2 * n + vpad));
+  h->vstride = (n + 31) / 32 * 32;
+  const int64_t vs = h->vstride;
+  A(dalloc(&h->pinv6, 6 * vs + vpad));
   for (int b = 0; b < 2; ++b) {
     A(dalloc(&h->ckey[b], ent2));
     A(dalloc(&h->cval[b], ent2));
@@ -249,10 +251,10 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->hck, std::max<int64_t>(mc, 1)));
   A(dalloc(&h->hcr, std::max<int64_t>(mc, 1)));
   A(dalloc(&h->dv, 3 * n + vpad));
-  A(dalloc(&h->dv4, n + vpad));
-  A(dalloc(&h->r4, n + vpad));
-  A(dalloc(&h->z4, n + vpad));
-  A(dalloc(&h->q4, n + vpad));
+  A(dalloc(&h->dv3, 3 * vs + vpad));
+  A(dalloc(&h->r3, 3 * vs + vpad));
+  A(dalloc(&h->z3, 3 * vs + vpad));
+  A(dalloc(&h->q3, 3 * vs + vpad));
   A(dalloc(&h->p4, n + vpad));
   A(dalloc(&h->rec, int64_t(h->loop_grid) * kRecSlots));
   A(dalloc(&h->bar, 1));
@@ -283,9 +285,10 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   if (e == cudaSuccess) e = cudaMemset(h->rowptr, 0, (n + 1 + vpad) * 4);
   for (float* v : {h->dv, h->rhs})
     if (e == cudaSuccess) e = cudaMemset(v, 0, (3 * n + vpad) * 4);
-  for (float4* v : {h->dv4, h->r4, h->z4, h->q4, h->p4})
-    if (e == cudaSuccess) e = cudaMemset(v, 0, (n + vpad) * sizeof(float4));
-  if (e == cudaSuccess) e = cudaMemset(h->pinv8, 0, (2 * n + vpad) * sizeof(float4));
+  for (float* v : {h->dv3, h->r3, h->z3, h->q3})
+    if (e == cudaSuccess) e = cudaMemset(v, 0, (3 * vs + vpad) * sizeof(float));
+  if (e == cudaSuccess) e = cudaMemset(h->p4, 0, (n + vpad) * sizeof(float4));
+  if (e == cudaSuccess) e = cudaMemset(h->pinv6, 0, (6 * vs + vpad) * sizeof(float));
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->state, 0, sizeof(PcgState));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();

@@ -59,7 +59,8 @@ struct AsmArgs {
   int32_t* colind;
   float* vals;
   float* rhs;
-  float4* pinv8;
+  float* pinv6;      // [6][vs]
+  int64_t vs;
   uint32_t* status;
 };
 
@@ -348,9 +349,13 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const fl
   const float c22 = d00 * d11 - d01 * d01;
   const float det = d00 * c00 + d01 * c01 + d02 * c02;
   const float id = 1.0f / det;
-  // the inverse of a symmetric block is symmetric: six entries, two float4
-  a.pinv8[2 * int64_t(i)] = make_float4(c00 * id, c01 * id, c02 * id, c11 * id);
-  a.pinv8[2 * int64_t(i) + 1] = make_float4(c12 * id, c22 * id, 0.f, 0.f);
+  // the inverse of a symmetric block is symmetric: six entries, one plane each
+  a.pinv6[i] = c00 * id;
+  a.pinv6[a.vs + i] = c01 * id;
+  a.pinv6[2 * a.vs + i] = c02 * id;
+  a.pinv6[3 * a.vs + i] = c11 * id;
+  a.pinv6[4 * a.vs + i] = c12 * id;
+  a.pinv6[5 * a.vs + i] = c22 * id;
   bool ok = finite3(b0, b1, b2) && isfinite(det) && det > 0.0f;
 #pragma unroll
   for (int t = 0; t < kSymBlock; ++t) ok = ok && isfinite(D[t]);
@@ -517,14 +522,16 @@ assemble_rows(AsmArgs a) {
   }
 }
 
-__global__ void pinv_expand(int32_t n, const float4* __restrict__ p8, float* __restrict__ out) {
+__global__ void pinv_expand(int32_t n, const float* __restrict__ p6, int64_t vs,
+                            float* __restrict__ out) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  const float4 u = p8[2 * i], w = p8[2 * i + 1];
+  const float p00 = p6[i], p01 = p6[vs + i], p02 = p6[2 * vs + i];
+  const float p11 = p6[3 * vs + i], p12 = p6[4 * vs + i], p22 = p6[5 * vs + i];
   float* o = out + 9 * i;
-  o[0] = u.x; o[1] = u.y; o[2] = u.z;
-  o[3] = u.y; o[4] = u.w; o[5] = w.x;
-  o[6] = u.z; o[7] = w.x; o[8] = w.y;
+  o[0] = p00; o[1] = p01; o[2] = p02;
+  o[3] = p01; o[4] = p11; o[5] = p12;
+  o[6] = p02; o[7] = p12; o[8] = p22;
 }
 
 // Packed symmetric blocks (a00 a01 a02 a11 a12 a22) to row-major 3x3.
@@ -549,7 +556,7 @@ int launch_vals_expand(Handle* h, float* out9, int64_t nnzb) {
 }
 
 int launch_pinv_expand(Handle* h, float* out9) {
-  pinv_expand<<<(h->n + 255) / 256, 256, 0, h->stream>>>(h->n, h->pinv8, out9);
+  pinv_expand<<<(h->n + 255) / 256, 256, 0, h->stream>>>(h->n, h->pinv6, h->vstride, out9);
   h->launches += 1;
   return check_launch(h, "pinv expand");
 }
@@ -614,7 +621,8 @@ int assemble_system(Handle* h, const float* x, const float* v,
   a.colind = h->colind;
   a.vals = h->vals;
   a.rhs = h->rhs;
-  a.pinv8 = h->pinv8;
+  a.pinv6 = h->pinv6;
+  a.vs = h->vstride;
   a.status = h->d_status;
   assemble_rows<<<ntiles, kAsmThreads, 0, s>>>(a);
   h->launches += 1;

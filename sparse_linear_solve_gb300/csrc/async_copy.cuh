@@ -66,19 +66,13 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
-// 16-byte global load / store with an L2 eviction-priority policy.
+// 16-byte global load with an L2 eviction-priority policy.
 __device__ __forceinline__ float4 ld_policy(const float4* p, uint64_t pol) {
   float4 v;
   asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p), "l"(pol));
   return v;
-}
-
-__device__ __forceinline__ void st_policy(float4* p, float4 v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
-               : "memory");
 }
 
 // Bulk copy of `bytes` (multiple of 16) from 16-byte aligned global memory to

@@ -38,22 +38,39 @@
 namespace pcloth_impl {
 namespace {
 
-// Accesses of the solver's vectors (p, q, r, z, dv, P: about 93 MB on the
-// largest cloth, less than L2) carry an L2 evict-last policy, so that the
-// matrix streamed past them (evict-first) does not push them out.
+// The SpMV's gathers of p carry an L2 evict-last policy, so that the matrix
+// streamed past them (evict-first) does not push p out.
 struct Vec {
   uint64_t pol;
   __device__ __forceinline__ float4 ld(const float4* p) const { return ld_policy(p, pol); }
-  __device__ __forceinline__ void st(float4* p, float4 v) const { st_policy(p, v, pol); }
 };
 
 __device__ __forceinline__ Vec vec_access() { return Vec{policy_evict_last()}; }
 
-__device__ __forceinline__ float3 apply_p(float4 u, float4 w, float3 r) {
-  // P = [[u.x u.y u.z] [u.y u.w w.x] [u.z w.x w.y]]
-  return make_float3(fmaf(u.x, r.x, fmaf(u.y, r.y, u.z * r.z)),
-                     fmaf(u.y, r.x, fmaf(u.w, r.y, w.x * r.z)),
-                     fmaf(u.z, r.x, fmaf(w.x, r.y, w.y * r.z)));
+// Row i of a vector stored as three planes (x, y, z) of vs floats.
+__device__ __forceinline__ float3 ld3(const float* __restrict__ v, int64_t vs, int64_t i) {
+  return make_float3(v[i], v[vs + i], v[2 * vs + i]);
+}
+
+__device__ __forceinline__ void st3(float* __restrict__ v, int64_t vs, int64_t i, float3 x) {
+  v[i] = x.x;
+  v[vs + i] = x.y;
+  v[2 * vs + i] = x.z;
+}
+
+// The symmetric block-Jacobi inverse of row i, stored as six planes.
+struct Sym3 {
+  float p00, p01, p02, p11, p12, p22;
+};
+
+__device__ __forceinline__ Sym3 ld_sym(const float* __restrict__ v, int64_t vs, int64_t i) {
+  return Sym3{v[i], v[vs + i], v[2 * vs + i], v[3 * vs + i], v[4 * vs + i], v[5 * vs + i]};
+}
+
+__device__ __forceinline__ float3 apply_p(const Sym3& P, float3 r) {
+  return make_float3(fmaf(P.p00, r.x, fmaf(P.p01, r.y, P.p02 * r.z)),
+                     fmaf(P.p01, r.x, fmaf(P.p11, r.y, P.p12 * r.z)),
+                     fmaf(P.p02, r.x, fmaf(P.p12, r.y, P.p22 * r.z)));
 }
 
 __device__ __forceinline__ float dot3(float3 a, float3 b) {
@@ -109,12 +126,13 @@ constexpr int kTileCache = 256;   // tiles per CTA whose block ranges stay in sh
 struct LoopArgs {
   PipeMatrix m;
   const float* b;          // float[n][3]
-  const float4* pinv8;     // 2 per vertex
-  float4* dv;
-  float4* r;
-  float4* z;
-  float4* p;
-  float4* q;
+  const float* pinv;       // [6][vs] planes P00 P01 P02 P11 P12 P22
+  float* dv;               // [3][vs] planes x, y, z
+  float* r;                // [3][vs]
+  float* z;                // [3][vs]
+  float4* p;               // one float4 per vertex: the SpMV gathers it
+  float* q;                // [3][vs]
+  int64_t vs;              // floats per plane
   float2* rec;             // [gridDim.x][kRecSlots]
   unsigned long long* bar; // grid-barrier counter, zero at launch
   PcgState* state;
@@ -142,13 +160,14 @@ struct PGather {
 
 struct PEpi {
   const float4* p;
-  float4* q;
+  float* q;
+  int64_t vs;
   Vec vm;
   float pq;
   float4 pr;   // p of this thread's row, loaded when its tile starts
   __device__ __forceinline__ void begin(int32_t row) { pr = vm.ld(p + row); }
   __device__ __forceinline__ void operator()(int32_t row, float3 acc) {
-    vm.st(q + row, make_float4(acc.x, acc.y, acc.z, 0.f));
+    st3(q, vs, row, acc);
     pq = fmaf(pr.x, acc.x, fmaf(pr.y, acc.y, fmaf(pr.z, acc.z, pq)));
   }
 };
@@ -203,12 +222,11 @@ pcg_loop(LoopArgs a) {
       if (i >= n) continue;
       const float3 bv = make_float3(a.b[3 * int64_t(i)], a.b[3 * int64_t(i) + 1],
                                     a.b[3 * int64_t(i) + 2]);
-      const float3 zv = apply_p(a.pinv8[2 * int64_t(i)], a.pinv8[2 * int64_t(i) + 1], bv);
-      const float4 z4 = make_float4(zv.x, zv.y, zv.z, 0.f);
-      a.r[i] = make_float4(bv.x, bv.y, bv.z, 0.f);
-      a.z[i] = z4;
-      a.p[i] = z4;
-      a.dv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float3 zv = apply_p(ld_sym(a.pinv, a.vs, i), bv);
+      st3(a.r, a.vs, i, bv);
+      st3(a.z, a.vs, i, zv);
+      a.p[i] = make_float4(zv.x, zv.y, zv.z, 0.f);
+      st3(a.dv, a.vs, i, make_float3(0.f, 0.f, 0.f));
       rz += dot3(bv, zv);
       bb += dot3(bv, bv);
     }
@@ -270,7 +288,7 @@ pcg_loop(LoopArgs a) {
     } else {
       const Vec vm = vec_access();
       PGather g{a.p, vm};
-      PEpi e{a.p, a.q, vm, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+      PEpi e{a.p, a.q, a.vs, vm, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
       if (!consumer_pass<BW>(C, sh, g, e)) atomicOr(a.status, ST_WAIT_TIMEOUT);
       pq = e.pq;
     }
@@ -313,21 +331,22 @@ pcg_loop(LoopArgs a) {
     {
       float arz = 0.f, arr = 0.f;
       {
-        const float4* __restrict__ qv_ = a.q;
-        const float4* __restrict__ pinv = a.pinv8;
-        float4* __restrict__ rv_ = a.r;
-        float4* __restrict__ zv_ = a.z;
+        const float* __restrict__ qv_ = a.q;
+        const float* __restrict__ pinv = a.pinv;
+        float* __restrict__ rv_ = a.r;
+        float* __restrict__ zv_ = a.z;
+        const int64_t vs = a.vs;
 #pragma unroll 2
         for (int32_t f = tid; f < nslots; f += kPipeThreads) {
           const int32_t i = own_row(f);
           if (i >= n) break;   // rows grow with f: the rest are past the end too
-          const float4 qv = qv_[i], rv = rv_[i];
-          const float4 pu = pinv[2 * int64_t(i)], pw = pinv[2 * int64_t(i) + 1];
+          const float3 qv = ld3(qv_, vs, i), rv = ld3(rv_, vs, i);
+          const Sym3 P = ld_sym(pinv, vs, i);
           const float3 rn = make_float3(fmaf(-alpha, qv.x, rv.x), fmaf(-alpha, qv.y, rv.y),
                                         fmaf(-alpha, qv.z, rv.z));
-          const float3 zn = apply_p(pu, pw, rn);
-          rv_[i] = make_float4(rn.x, rn.y, rn.z, 0.f);
-          zv_[i] = make_float4(zn.x, zn.y, zn.z, 0.f);
+          const float3 zn = apply_p(P, rn);
+          st3(rv_, vs, i, rn);
+          st3(zv_, vs, i, zn);
           arz += dot3(rn, zn);
           arr += dot3(rn, rn);
         }
@@ -390,16 +409,18 @@ pcg_loop(LoopArgs a) {
     {
       const float beta = scal_sh;
       float4* __restrict__ pv_ = a.p;
-      float4* __restrict__ dv_ = a.dv;
-      const float4* __restrict__ zv_ = a.z;
+      float* __restrict__ dv_ = a.dv;
+      const float* __restrict__ zv_ = a.z;
+      const int64_t vs = a.vs;
 #pragma unroll 2
       for (int32_t f = tid; f < nslots; f += kPipeThreads) {
         const int32_t i = own_row(f);
         if (i >= n) break;
-        const float4 pv = pv_[i], dvv = dv_[i];
-        const float4 zv = stop ? pv : zv_[i];
-        dv_[i] = make_float4(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
-                             fmaf(alpha, pv.z, dvv.z), 0.f);
+        const float4 pv = pv_[i];
+        const float3 dvv = ld3(dv_, vs, i);
+        const float3 zv = stop ? make_float3(pv.x, pv.y, pv.z) : ld3(zv_, vs, i);
+        st3(dv_, vs, i, make_float3(fmaf(alpha, pv.x, dvv.x), fmaf(alpha, pv.y, dvv.y),
+                                    fmaf(alpha, pv.z, dvv.z)));
         if (!stop)
           pv_[i] = make_float4(fmaf(beta, pv.x, zv.x), fmaf(beta, pv.y, zv.y),
                                fmaf(beta, pv.z, zv.z), 0.f);
@@ -427,7 +448,7 @@ pcg_loop(LoopArgs a) {
   for (int32_t f = tid; f < nslots; f += kPipeThreads) {
     const int32_t i = own_row(f);
     if (i >= n) continue;
-    const float4 d = a.dv[i];
+    const float3 d = ld3(a.dv, a.vs, i);
     a.dv_out[3 * int64_t(i)] = d.x;
     a.dv_out[3 * int64_t(i) + 1] = d.y;
     a.dv_out[3 * int64_t(i) + 2] = d.z;
@@ -512,12 +533,13 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
   a.m = PipeMatrix{h->n, (h->n + kPipeRows - 1) / kPipeRows, h->rowptr, h->colind, h->vals,
                    nullptr, 0};
   a.b = h->rhs;
-  a.pinv8 = h->pinv8;
-  a.dv = h->dv4;
-  a.r = h->r4;
-  a.z = h->z4;
+  a.pinv = h->pinv6;
+  a.dv = h->dv3;
+  a.r = h->r3;
+  a.z = h->z3;
   a.p = h->p4;
-  a.q = h->q4;
+  a.q = h->q3;
+  a.vs = h->vstride;
   a.rec = h->rec;
   a.bar = h->bar;
   a.state = h->state;
@@ -574,7 +596,7 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
 // cudaMalloc, cudaFree or any allocating routine.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
-// library holds it (about 2.2 MiB) until the process exits, and every call
+// library holds it (about 1.5 MiB) until the process exits, and every call
 // on that GPU shares it.  Calls that overlap on the GPU therefore race on it;
 // a caller must order them (one stream, or events).  Each call re-initialises
 // everything it reads before reading it, so nothing leaks from one call into
@@ -582,25 +604,28 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
 // ===========================================================================
 namespace {
 
-constexpr int64_t kStaticVec = int64_t(PCLOTH_STATIC_MAX_VERTS) + 64;  // float4 per vector
-constexpr int kStaticMaxRecords = 2048;                                 // CTAs of the solve
-constexpr size_t kStaticBytes =
-    sizeof(float4) * size_t(2 * kStaticVec        // block-Jacobi inverses (2 per vertex)
-                            + 5 * kStaticVec      // dv, r, z, p, q
-                            + kStaticVec)         // spare
-    + sizeof(float2) * size_t(kRecSlots) * size_t(kStaticMaxRecords) + 256;
+constexpr int64_t kStaticVec = int64_t(PCLOTH_STATIC_MAX_VERTS) + 64;   // float4 slots of p
+constexpr int64_t kStaticPlane =                                          // floats per plane
+    (int64_t(PCLOTH_STATIC_MAX_VERTS) + 31) / 32 * 32 + 64;
+constexpr int kStaticPlanes = 6 + 4 * 3;   // P; dv, r, z, q
+constexpr int kStaticMaxRecords = 2048;    // CTAs of the solve
+constexpr size_t kStaticBytes = sizeof(float4) * size_t(kStaticVec) +
+                                sizeof(float) * size_t(kStaticPlanes) * size_t(kStaticPlane) +
+                                sizeof(float2) * size_t(kRecSlots) * size_t(kStaticMaxRecords) +
+                                256;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
 // Device address of g_static_scratch per device ordinal (set up on first use).
 void* g_static_addr[64] = {};
 
-// Inverse of the diagonal block of each row of a caller's BSR3 matrix, packed
-// like the library's own: (P00 P01 P02 P11) (P12 P22 0 0).  A row without a
+// Inverse of the diagonal block of each row of a caller's BSR3 matrix, stored
+// like the library's own: six planes P00 P01 P02 P11 P12 P22 of vs floats.  A row without a
 // diagonal block, or with a non-invertible one, is reported as non-finite.
 __global__ void bsr3_diag_inverse(int32_t n, const int32_t* __restrict__ rowptr,
                                   const int32_t* __restrict__ colind,
-                                  const float* __restrict__ vals, float4* __restrict__ pinv8,
+                                  const float* __restrict__ vals, float* __restrict__ pinv6,
+                                  int64_t vs,
                                   uint32_t* status) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
@@ -625,8 +650,12 @@ __global__ void bsr3_diag_inverse(int32_t n, const int32_t* __restrict__ rowptr,
     det = 1.f;
   }
   const float id = 1.0f / det;
-  pinv8[2 * i] = make_float4(c00 * id, c01 * id, c02 * id, c11 * id);
-  pinv8[2 * i + 1] = make_float4(c12 * id, c22 * id, 0.f, 0.f);
+  pinv6[i] = c00 * id;
+  pinv6[vs + i] = c01 * id;
+  pinv6[2 * vs + i] = c02 * id;
+  pinv6[3 * vs + i] = c11 * id;
+  pinv6[4 * vs + i] = c12 * id;
+  pinv6[5 * vs + i] = c22 * id;
 }
 
 }  // namespace
@@ -655,19 +684,21 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
   if (grid > kStaticMaxRecords)
     return fail(nullptr, PCLOTH_ERR_CAPACITY, "too many CTAs for the fixed partial sums");
   unsigned char* base = static_cast<unsigned char*>(g_static_addr[device]);
-  float4* v4 = reinterpret_cast<float4*>(base);
-  float2* rec = reinterpret_cast<float2*>(v4 + 8 * kStaticVec);
+  float4* p4 = reinterpret_cast<float4*>(base);
+  float* planes = reinterpret_cast<float*>(p4 + kStaticVec);
+  float2* rec = reinterpret_cast<float2*>(planes + size_t(kStaticPlanes) * kStaticPlane);
   unsigned char* tail = reinterpret_cast<unsigned char*>(rec + size_t(kRecSlots) * kStaticMaxRecords);
   LoopArgs a{};
   a.m = PipeMatrix{n, (n + kPipeRows - 1) / kPipeRows, rowptr, colind, vals, nullptr, 0};
   a.b = b;
-  float4* pinv8 = v4;
-  a.pinv8 = pinv8;
-  a.dv = v4 + 2 * kStaticVec;
-  a.r = v4 + 3 * kStaticVec;
-  a.z = v4 + 4 * kStaticVec;
-  a.p = v4 + 5 * kStaticVec;
-  a.q = v4 + 6 * kStaticVec;
+  float* pinv6 = planes;
+  a.pinv = pinv6;
+  a.dv = planes + 6 * kStaticPlane;
+  a.r = planes + 9 * kStaticPlane;
+  a.z = planes + 12 * kStaticPlane;
+  a.q = planes + 15 * kStaticPlane;
+  a.p = p4;
+  a.vs = kStaticPlane;
   a.rec = rec;
   a.state = reinterpret_cast<PcgState*>(tail);
   uint32_t* status = reinterpret_cast<uint32_t*>(tail + 64);
@@ -680,8 +711,8 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
 
   e = cudaMemsetAsync(tail, 0, 256, stream);   // state, status and barrier counter
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve reset");
-  bsr3_diag_inverse<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, vals, pinv8,
-                                                        status);
+  bsr3_diag_inverse<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, vals, pinv6,
+                                                        kStaticPlane, status);
   e = cudaGetLastError();
   if (e == cudaSuccess) e = launch_loop<9>(a, grid, stream);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve launch");

@@ -100,7 +100,7 @@ struct Handle {
   float* vals = nullptr;         // nnzb_cap*blk (+pad)
   int32_t blk = kSymBlock;       // floats per block in vals
   float* rhs = nullptr;          // 3n
-  float4* pinv8 = nullptr;       // 2 per vertex: (P00 P01 P02 P11) (P12 P22 0 0)
+  float* pinv6 = nullptr;        // [6][vstride] planes P00 P01 P02 P11 P12 P22
 
   // per-step contact workspace (capacity 2*max_contacts entries)
   uint64_t* ckey[2] = {nullptr, nullptr};
@@ -127,14 +127,18 @@ struct Handle {
   float* hck = nullptr;
   float* hcr = nullptr;
 
-  // PCG workspace: one float4 (x, y, z, 0) per vertex, so that a gather is
-  // one aligned 16-byte load and the vector phases are fully coalesced
+  // PCG workspace.  p, which the SpMV gathers, holds one float4 (x, y, z, 0)
+  // per vertex, so that a gather is one aligned 16-byte load.  The vectors
+  // that are only read and written row by row are three planes (x, y, z) of
+  // vstride floats each, so that a warp's loads and stores cover whole
+  // sectors and move no padding.
   float* dv = nullptr;             // float[n][3] scratch (pcloth_step without dv)
-  float4* dv4 = nullptr;
-  float4* r4 = nullptr;
-  float4* z4 = nullptr;
+  int64_t vstride = 0;             // floats per plane: n rounded up to 32
+  float* dv3 = nullptr;            // [3][vstride]
+  float* r3 = nullptr;
+  float* z3 = nullptr;
+  float* q3 = nullptr;
   float4* p4 = nullptr;
-  float4* q4 = nullptr;
   float2* rec = nullptr;           // loop_grid * kRecSlots partial sums
   unsigned long long* bar = nullptr;       // grid-barrier arrival counter
   unsigned long long* phase_ns = nullptr;  // [4] phase times of the last solve
