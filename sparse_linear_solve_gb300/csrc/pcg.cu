@@ -21,10 +21,10 @@
 // Every scalar is formed by every CTA from the same per-CTA partials in the
 // same order (double-float sums), so all CTAs take the same decisions and
 // the solve is bitwise reproducible.  No host round trip happens inside the
-// solve.  The matrix does not change during a solve, so once the P phase
-// has decided to go on, the producer lane already issues the first stages
-// of the next SpMV; their loads overlap the rest of the P phase and the
-// barrier.
+// solve.  The U phase loads its first row's inputs, which do not depend on
+// alpha, before it reduces p.q.  The vector phases are bound by memory
+// bandwidth, so the next SpMV's copies are not issued early: they would
+// compete with them.
 //
 // Every wait (mbarrier, grid barrier) is bounded in time: on a timeout the
 // kernel records ST_WAIT_TIMEOUT, waits (bounded) for its own copies in
@@ -306,6 +306,15 @@ pcg_loop(LoopArgs a) {
     }
 
     // ---- U: alpha; r, z; partials r.z, r.r ----------------------------------
+    // the first row's inputs do not depend on alpha: load them under the reduction
+    const int32_t i_first = tid < nslots ? own_row(tid) : n;
+    float3 q_first = make_float3(0.f, 0.f, 0.f), r_first = q_first;
+    Sym3 p_first{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (i_first < n) {
+      q_first = ld3(a.q, a.vs, i_first);
+      r_first = ld3(a.r, a.vs, i_first);
+      p_first = ld_sym(a.pinv, a.vs, i_first);
+    }
     {
       Dfloat v[1] = {records_share(a.rec, gridDim.x, REC_PQ, kPipeThreads)};
       block_sum_df<kPipeThreads, 1>(v, red_sh);
@@ -336,8 +345,18 @@ pcg_loop(LoopArgs a) {
         float* __restrict__ rv_ = a.r;
         float* __restrict__ zv_ = a.z;
         const int64_t vs = a.vs;
+        if (i_first < n) {
+          const float3 rn = make_float3(fmaf(-alpha, q_first.x, r_first.x),
+                                        fmaf(-alpha, q_first.y, r_first.y),
+                                        fmaf(-alpha, q_first.z, r_first.z));
+          const float3 zn = apply_p(p_first, rn);
+          st3(rv_, vs, i_first, rn);
+          st3(zv_, vs, i_first, zn);
+          arz += dot3(rn, zn);
+          arr += dot3(rn, rn);
+        }
 #pragma unroll 2
-        for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+        for (int32_t f = tid + kPipeThreads; f < nslots; f += kPipeThreads) {
           const int32_t i = own_row(f);
           if (i >= n) break;   // rows grow with f: the rest are past the end too
           const float3 qv = ld3(qv_, vs, i), rv = ld3(rv_, vs, i);
@@ -394,12 +413,6 @@ pcg_loop(LoopArgs a) {
         stop_sh = stop;
         L.rr_last = rr;
         L.rz_old = rz;
-        if (!stop) {
-          Producer P = L.P;
-          for (int j = 0; j < kPipeStages && !P.ended; ++j)
-            if (producer_step<BW>(P, sh, m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
-          L.P = P;
-        }
       }
       __syncthreads();
     }
