@@ -32,6 +32,8 @@ namespace pcloth_impl {
 namespace {
 
 constexpr uint64_t kSentinel = ~0ull;
+constexpr int kRowLanes = kAsmThreads / kAsmRows;   // threads per row in the row reductions
+static_assert(kRowLanes == 8, "the row reduction merges eight lanes");
 
 struct AsmArgs {
   int32_t n;
@@ -173,11 +175,32 @@ __device__ __forceinline__ Edge edge_of(float3 xi, float3 xj) {
   return e;
 }
 
-// |e|^2 - L0^2 in fp64 from an exact edge (hi + lo is exact in fp64 and its
-// square is accurate to fp64 rounding).
-__device__ __forceinline__ double excess_sq(float3 hi, float3 lo, float L0) {
-  const double x = double(hi.x) + lo.x, y = double(hi.y) + lo.y, z = double(hi.z) + lo.z;
-  return x * x + y * y + z * z - double(L0) * L0;
+// |e|^2 - L0^2 from an exact edge e = hi + lo, in fp32 pairs: the four large
+// terms hi.x^2, hi.y^2, hi.z^2 and -L0^2 are split exactly into product and
+// residual by an FMA and the products summed by TwoSum, so the cancellation
+// near the rest length loses nothing; the residuals, the cross terms
+// 2 hi.lo and lo.lo (all about 2^-24 of the squares or smaller) are added in
+// plain fp32.  The error is about 2^-48 |e|^2, like an fp64 evaluation, at
+// fp32 speed (fp64 is a slow path on this GPU).  Every term is even in e, so
+// the edges e and -e give the same bits.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& t) {
+  s = a + b;
+  const float bp = s - a;
+  t = (a - (s - bp)) + (b - bp);
+}
+
+__device__ __forceinline__ float excess_sq(float3 hi, float3 lo, float L0) {
+  const float px = hi.x * hi.x, py = hi.y * hi.y, pz = hi.z * hi.z, pl = -(L0 * L0);
+  const float rx = fmaf(hi.x, hi.x, -px), ry = fmaf(hi.y, hi.y, -py);
+  const float rz = fmaf(hi.z, hi.z, -pz), rl = fmaf(-L0, L0, -pl);
+  float s, t1, t2, t3;
+  two_sum(px, py, s, t1);
+  two_sum(s, pz, s, t2);
+  two_sum(s, pl, s, t3);
+  const float cross = 2.0f * fmaf(hi.x, lo.x, fmaf(hi.y, lo.y, hi.z * lo.z)) +
+                      fmaf(lo.x, lo.x, fmaf(lo.y, lo.y, lo.z * lo.z));
+  const float small = ((t1 + t2) + t3) + (((rx + ry) + rz) + rl) + cross;
+  return s + small;
 }
 
 // Scaled stiffness block K' = -h^2 K (6 unique entries of the symmetric
@@ -187,7 +210,7 @@ __device__ __forceinline__ double excess_sq(float3 hi, float3 lo, float L0) {
 //
 // K = a I + c d d^T with a = k max(0, 1 - L0/l), c = k - a.  The length
 // excess l - L0 is formed as (|e|^2 - L0^2) / (l + L0) with the squares in
-// fp64: near the rest length the plain fp32 difference is pure rounding noise
+// fp32 pairs: near the rest length the plain fp32 difference is pure rounding noise
 // (~1e-7 L0) that would give a spring at rest a spurious transverse stiffness
 // along exactly the soft out-of-plane directions of a flat sheet.  Written
 // as K' = A I + S e e^T with A = -h^2 a and S = -h^2 c / l^2, each product
@@ -212,7 +235,7 @@ __device__ __forceinline__ void element_terms(const Edge& e, float3 w, float dt,
   const float l2 = fmaf(h.x, h.x, fmaf(h.y, h.y, h.z * h.z)) +
                    2.0f * fmaf(h.x, o.x, fmaf(h.y, o.y, h.z * o.z));
   const float l = sqrtf(l2);
-  const float stretch = float(excess_sq(h, o, L0)) / (l + L0);    // l - L0
+  const float stretch = excess_sq(h, o, L0) / (l + L0);    // l - L0
   const float tension = fmaxf(0.0f, stretch / l);                  // max(0, 1 - L0/l)
   const float a = k * tension;
   const float c = k - a;
@@ -229,7 +252,7 @@ __device__ __forceinline__ void element_terms(const Edge& e, float3 w, float dt,
               fz = fmaf(dt, w.z, h.z) + o.z;
   const float lt = sqrtf(fx * fx + fy * fy + fz * fz);
   const float3 fz3 = make_float3(0.f, 0.f, 0.f);
-  const float st = float(excess_sq(make_float3(fx, fy, fz), fz3, L0)) / (lt + L0);   // l~ - L0
+  const float st = excess_sq(make_float3(fx, fy, fz), fz3, L0) / (lt + L0);   // l~ - L0
   const float s = k * st / lt;
   F[0] += s * fx;
   F[1] += s * fy;
@@ -362,7 +385,10 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const fl
   if (!ok) atomicOr(a.status, ST_NONFINITE);
 }
 
-__global__ void __launch_bounds__(kAsmThreads)
+// Four CTAs per SM (64 registers a thread): the kernel is bound by the
+// latency of its gathers and of the per-row reductions, so occupancy pays
+// more than the few spills it costs.
+__global__ void __launch_bounds__(kAsmThreads, 4)
 assemble_rows(AsmArgs a) {
   __shared__ RowInfo rows[kAsmRows + 1];
   __shared__ float stv[kAsmCap * kSymBlock];
@@ -425,34 +451,63 @@ assemble_rows(AsmArgs a) {
                       m_valid);
       }
       __syncthreads();
-      // phase 3: one thread per row reduces its blocks into the diagonal
-      for (int32_t ri = g + threadIdx.x; ri < e; ri += kAsmThreads) {
+      // phase 3: eight threads per row (kAsmRows x 8 = kAsmThreads) reduce
+      // its blocks into the diagonal.  h^2 sum K is compensated (TwoSum):
+      // the diagonal is ~h^2 k while the mass it must preserve is far
+      // smaller.  Thread q of a row takes blocks q, q + 8, ... in column
+      // order; the eight (sum, compensation) pairs are then merged by a
+      // butterfly whose steps are commutative, so the order is fixed and
+      // all eight threads hold the same bits.
+      {
+        const int32_t ri = g + int32_t(threadIdx.x) / kRowLanes;
+        const int32_t q = int32_t(threadIdx.x) % kRowLanes;
+        const bool live = ri < e;
         const int32_t i = r0 + ri;
-        const int32_t o0 = rows[ri].ob - gob, o1 = rows[ri + 1].ob - gob;
-        // h^2 sum K over the row, compensated (TwoSum): the diagonal is
-        // ~h^2 k while the mass it must preserve is far smaller
         float Ks[6] = {0, 0, 0, 0, 0, 0}, Kc[6] = {0, 0, 0, 0, 0, 0}, Fs[3] = {0, 0, 0};
         int32_t dpos = -1;
-        for (int32_t o = o0; o < o1; ++o) {
-          if (stc[o] == i) { dpos = o; continue; }
-          const float* s = &stv[kSymBlock * o];
+        if (live) {
+          const int32_t o0 = rows[ri].ob - gob, o1 = rows[ri + 1].ob - gob;
+          for (int32_t o = o0 + q; o < o1; o += kRowLanes) {
+            if (stc[o] == i) { dpos = o; continue; }
+            const float* sv = &stv[kSymBlock * o];
+#pragma unroll
+            for (int t = 0; t < 6; ++t) {
+              const float x = -sv[t];
+              const float sum = Ks[t] + x;
+              const float bp = sum - Ks[t];
+              Kc[t] += (Ks[t] - (sum - bp)) + (x - bp);
+              Ks[t] = sum;
+            }
+            Fs[0] += stf[3 * o]; Fs[1] += stf[3 * o + 1]; Fs[2] += stf[3 * o + 2];
+          }
+        }
+#pragma unroll
+        for (int off = kRowLanes / 2; off > 0; off >>= 1) {
 #pragma unroll
           for (int t = 0; t < 6; ++t) {
-            const float x = -s[t];
-            const float sum = Ks[t] + x;
+            const float so = __shfl_xor_sync(0xffffffffu, Ks[t], off);
+            const float co = __shfl_xor_sync(0xffffffffu, Kc[t], off);
+            // TwoSum's error is the exact rounding error of the sum, so
+            // both lanes of the pair get the same bits in either order
+            const float sum = Ks[t] + so;
             const float bp = sum - Ks[t];
-            Kc[t] += (Ks[t] - (sum - bp)) + (x - bp);
+            const float err = (Ks[t] - (sum - bp)) + (so - bp);
+            Kc[t] = (Kc[t] + co) + err;
             Ks[t] = sum;
           }
-          Fs[0] += stf[3 * o]; Fs[1] += stf[3 * o + 1]; Fs[2] += stf[3 * o + 2];
-        }
-        float D[kSymBlock];
-        finish_row(a, i, Ks, Kc, Fs, D);
-        if (dpos >= 0) {
 #pragma unroll
-          for (int t = 0; t < kSymBlock; ++t) stv[kSymBlock * dpos + t] = D[t];
-        } else {
-          atomicOr(a.status, ST_CAPACITY);  // diagonal missing: cannot happen
+          for (int t = 0; t < 3; ++t) Fs[t] += __shfl_xor_sync(0xffffffffu, Fs[t], off);
+          dpos = max(dpos, __shfl_xor_sync(0xffffffffu, dpos, off));
+        }
+        if (live && q == 0) {
+          float D[kSymBlock];
+          finish_row(a, i, Ks, Kc, Fs, D);
+          if (dpos >= 0) {
+#pragma unroll
+            for (int t = 0; t < kSymBlock; ++t) stv[kSymBlock * dpos + t] = D[t];
+          } else {
+            atomicOr(a.status, ST_CAPACITY);  // diagonal missing: cannot happen
+          }
         }
       }
       __syncthreads();
