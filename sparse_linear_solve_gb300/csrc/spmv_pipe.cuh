@@ -14,12 +14,15 @@
 //     of shared-memory stages with bulk asynchronous copies, completion
 //     counted on mbarriers, with an L2 evict-first hint so that the gathered
 //     vector stays L2-resident;
-//   * the consumer warps work in two phases per stage: one thread per block
-//     multiplies its block (packed symmetric or general, see block_times) by
-//     the gathered input vertex -- a thread issues all of its gathers before
-//     using any -- and stores the three products; then one thread per row
-//     adds its row's products in column order and hands the row to an
-//     epilogue.
+//   * the consumer warps have two roles.  Five product warps take one thread
+//     per block: it multiplies its block (packed symmetric or general, see
+//     block_times) by the gathered input vertex -- a thread issues all of
+//     its gathers before using any -- and stores the three products.  Two
+//     row warps take one thread per row of the tile: it adds its row's
+//     products in column order and hands the row to an epilogue.  The
+//     products are double-buffered and pass between the roles on mbarriers,
+//     so the row sums of one stage overlap the gathers of the next and are
+//     off the product warps' path.
 //
 // Tiles longer than a stage are split into chunks and the row sums carry
 // over, so every output has a fixed summation order and the product is
@@ -41,7 +44,9 @@ namespace pcloth_impl {
 // second stage); three stages keep two tiles' copies in flight while one is
 // consumed.  With packed blocks a CTA needs 103 KB of shared memory, so two
 // CTAs run per SM.  Measured on the 1.65M-triangle cloth, this beat 48-row
-// tiles of 640 blocks at 3 CTAs per SM by 15% per PCG iteration.
+// tiles of 640 blocks at 3 CTAs per SM by 15% per PCG iteration.  Seven
+// consumer warps (five product, two row) beat six, eight, nine and ten per
+// PCG iteration: a CTA of 256 threads keeps 128 registers a thread.
 #ifndef PCLOTH_PIPE_ROWS
 #define PCLOTH_PIPE_ROWS 64
 #endif
@@ -61,7 +66,10 @@ constexpr int kPipeRows = PCLOTH_PIPE_ROWS;   // rows per tile (multiple of 4)
 constexpr int kPipeCap = PCLOTH_PIPE_CAP;     // blocks per stage
 constexpr int kPipeStages = PCLOTH_PIPE_STAGES;
 constexpr int kPipeCtasPerSm = PCLOTH_PIPE_CTAS;
-constexpr int kPipeConsumerWarps = 8;
+#ifndef PCLOTH_PIPE_CWARPS
+#define PCLOTH_PIPE_CWARPS 7
+#endif
+constexpr int kPipeConsumerWarps = PCLOTH_PIPE_CWARPS;
 constexpr int kPipeConsumers = 32 * kPipeConsumerWarps;
 constexpr int kPipeThreads = 32 + kPipeConsumers;
 constexpr int kPipePerThread = (kPipeCap + kPipeConsumers - 1) / kPipeConsumers;
@@ -72,8 +80,16 @@ constexpr int kPipePartBytes = kPipeCap * 16; // one float4 of products per bloc
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legal wait
 static_assert(kPipeRows % 4 == 0, "row-pointer copies must start 16-byte aligned");
 static_assert(kPipeRows <= kPipeConsumers, "one consumer per row");
-static_assert(2 * kPipeStages * 8 <= 64 && 64 + kPipeStages * 32 <= kPipeHeadBytes,
-              "ring barriers at offset 0, stage descriptors at offset 64");
+static_assert(2 * kPipeStages * 8 <= 64 && 64 + kPipeStages * 32 + 32 <= kPipeHeadBytes,
+              "ring barriers at offset 0, stage descriptors at offset 64, then the four "
+              "product-buffer barriers");
+// The consumers split in two roles: kPipeProd threads form the block
+// products of a stage, kPipeRows threads (two warps) add the rows of the
+// stage before, and the double-buffered products pass between them on
+// mbarriers (ready: products written; free: products read).
+constexpr int kPipeProd = kPipeConsumers - kPipeRows;
+constexpr int kPipeProdPerThread = (kPipeCap + kPipeProd - 1) / kPipeProd;
+static_assert(kPipeProd % 32 == 0 && kPipeProd > 0, "whole warps per role");
 
 // Shared-memory geometry for blocks of BW floats: per stage the row
 // pointers, block values and column indices (each copy window has 16 bytes
@@ -141,6 +157,8 @@ struct PipeMatrix {
 struct PipeShared {
   uint64_t* full;
   uint64_t* empty;
+  uint64_t* ready;   // [2] products of a buffer written (kPipeProd arrivals)
+  uint64_t* freed;   // [2] products of a buffer read (kPipeRows arrivals)
   StageDesc* desc;
   unsigned char* stages;
   float4* parts;
@@ -152,6 +170,8 @@ __device__ __forceinline__ PipeShared pipe_shared(unsigned char* smem) {
   s.full = reinterpret_cast<uint64_t*>(smem);
   s.empty = s.full + kPipeStages;
   s.desc = reinterpret_cast<StageDesc*>(smem + 64);
+  s.ready = reinterpret_cast<uint64_t*>(smem + 64 + kPipeStages * 32);
+  s.freed = s.ready + 2;
   s.stages = smem + kPipeHeadBytes;
   s.parts = reinterpret_cast<float4*>(s.stages + size_t(kPipeStages) * Pipe<BW>::kStageBytes);
   return s;
@@ -163,6 +183,10 @@ __device__ __forceinline__ void pipe_init(const PipeShared& sh) {
     for (int s = 0; s < kPipeStages; ++s) {
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], kPipeConsumers);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.ready[b], kPipeProd);
+      mbar_init(&sh.freed[b], kPipeRows);
     }
     mbar_init_fence();
   }
@@ -322,7 +346,7 @@ __device__ __forceinline__ bool producer_pass(Producer& P, const PipeShared& sh,
 struct Consumer {
   int s;
   uint32_t ph;
-  int buf;
+  int buf;   // data stages consumed so far: buffer buf & 1, its (buf >> 1)-th use
 };
 
 __device__ __forceinline__ void consumer_begin(Consumer& C) {
@@ -333,13 +357,15 @@ __device__ __forceinline__ void consumer_begin(Consumer& C) {
 
 // Consumer side of one pass (threads 32 .. kPipeThreads-1): processes stages
 // up to and including the end marker.  gather(col) returns the input vertex
-// col as a float3; epi.begin(row) is called when a tile starts (before the
-// gathers, so loads it issues overlap them) and epi(row, acc) receives each
-// finished row's sum.  Returns false if a stage never arrived.
+// col as a float3; epi.begin(row) is called when a tile starts and epi(row,
+// acc) receives each finished row's sum (both in the row threads).  Returns
+// false if a stage, or the other role, never arrived.
 template <int BW, class Gather, class Epi>
 __device__ __forceinline__ bool consumer_pass(Consumer& C, const PipeShared& sh, Gather& gather,
                                               Epi& epi) {
   const int ct = threadIdx.x - 32;
+  const bool prod = ct < kPipeProd;
+  const int rt = ct - kPipeProd;    // row thread index (row threads only)
   float3 acc = make_float3(0.f, 0.f, 0.f);
   while (true) {
     if (!wait_bounded(&sh.full[C.s], C.ph)) return false;
@@ -350,49 +376,60 @@ __device__ __forceinline__ bool consumer_pass(Consumer& C, const PipeShared& sh,
       return true;
     }
     const unsigned char* st = sh.stages + size_t(C.s) * Pipe<BW>::kStageBytes;
-    const int32_t* rp = reinterpret_cast<const int32_t*>(st);
-    const float* sv = reinterpret_cast<const float*>(st + kPipeRpInts * 4) + d.voff;
-    const int32_t* sc =
-        reinterpret_cast<const int32_t*>(st + kPipeRpInts * 4 + Pipe<BW>::kValBytes) + d.coff;
-    float4* part = sh.parts + C.buf * kPipeCap;
-    const int32_t cn = d.c1 - d.c0;
-    const bool row_owner = ct < d.nrows;
-    if (row_owner && (d.flags & 1)) epi.begin(d.r0 + ct);
-    // phase B: block products, all of a thread's gathers in flight at once
-    {
-      int32_t col[kPipePerThread];
-      float3 xv[kPipePerThread];
+    const int b = C.buf & 1;
+    const uint32_t use = uint32_t(C.buf >> 1) & 1u;
+    float4* part = sh.parts + b * kPipeCap;
+    if (prod) {
+      const float* sv = reinterpret_cast<const float*>(st + kPipeRpInts * 4) + d.voff;
+      const int32_t* sc =
+          reinterpret_cast<const int32_t*>(st + kPipeRpInts * 4 + Pipe<BW>::kValBytes) + d.coff;
+      const int32_t cn = d.c1 - d.c0;
+      int32_t col[kPipeProdPerThread];
+      float3 xv[kPipeProdPerThread];
 #pragma unroll
-      for (int u = 0; u < kPipePerThread; ++u) {
-        const int j = ct + u * kPipeConsumers;
+      for (int u = 0; u < kPipeProdPerThread; ++u) {
+        const int j = ct + u * kPipeProd;
         col[u] = j < cn ? sc[j] : -1;
       }
 #pragma unroll
-      for (int u = 0; u < kPipePerThread; ++u)
+      for (int u = 0; u < kPipeProdPerThread; ++u)
         if (col[u] >= 0) xv[u] = gather(col[u]);
+      // the buffer is free once the row threads have added its last use
+      if (!wait_bounded(&sh.freed[b], use ^ 1u)) return false;
 #pragma unroll
-      for (int u = 0; u < kPipePerThread; ++u) {
-        const int j = ct + u * kPipeConsumers;
+      for (int u = 0; u < kPipeProdPerThread; ++u) {
+        const int j = ct + u * kPipeProd;
         if (col[u] >= 0) part[j] = block_times<BW>(sv + BW * j, xv[u]);
       }
-    }
-    named_barrier_sync(1, kPipeConsumers);
-    // phase C: row sums in column order, one thread per row
-    if (row_owner) {
-      const int32_t rs = max(rp[ct], d.c0) - d.c0, re = min(rp[ct + 1], d.c1) - d.c0;
-      for (int32_t j = rs; j < re; ++j) {
-        const float4 t = part[j];
-        acc.x += t.x;
-        acc.y += t.y;
-        acc.z += t.z;
+      mbar_arrive(&sh.empty[C.s]);   // this thread no longer reads the stage
+      mbar_arrive(&sh.ready[b]);
+    } else {
+      const int32_t* rp = reinterpret_cast<const int32_t*>(st);
+      const bool row_owner = rt < d.nrows;
+      int32_t rs = 0, re = 0;
+      if (row_owner) {
+        rs = max(rp[rt], d.c0) - d.c0;
+        re = min(rp[rt + 1], d.c1) - d.c0;
+        if (d.flags & 1) epi.begin(d.r0 + rt);
+      }
+      const int r0 = d.r0, last = d.flags & 2;
+      mbar_arrive(&sh.empty[C.s]);   // desc and row pointers read
+      if (!wait_bounded(&sh.ready[b], use)) return false;
+      if (row_owner) {
+        for (int32_t j = rs; j < re; ++j) {
+          const float4 t = part[j];
+          acc.x += t.x;
+          acc.y += t.y;
+          acc.z += t.z;
+        }
+      }
+      mbar_arrive(&sh.freed[b]);
+      if (row_owner && last) {
+        epi(r0 + rt, acc);
+        acc = make_float3(0.f, 0.f, 0.f);
       }
     }
-    mbar_arrive(&sh.empty[C.s]);   // this thread no longer reads the stage
-    if (row_owner && (d.flags & 2)) {
-      epi(d.r0 + ct, acc);
-      acc = make_float3(0.f, 0.f, 0.f);
-    }
-    C.buf ^= 1;
+    ++C.buf;
     if (++C.s == kPipeStages) { C.s = 0; C.ph ^= 1u; }
   }
 }
