@@ -232,7 +232,7 @@ int pcloth_profile_read(pcloth_t h, double* ms_out, int64_t* counts_out,
  * given stream (a cudaStream_t, 0 = legacy default), and returns
  * *iterations and *rel_residual on the host.  It allocates nothing: all of
  * its scratch is one fixed array compiled into this library, which every
- * GPU that loads the library holds (about 2.2 MiB) until the process exits.
+ * GPU that loads the library holds (about 1.5 MiB) until the process exits.
  * n may be at most PCLOTH_STATIC_MAX_VERTS; larger n returns
  * PCLOTH_ERR_CAPACITY without touching the GPU.  Every call on a device
  * shares that array, so calls that overlap on the GPU race: order them (one
@@ -244,6 +244,21 @@ int pcloth_solve_bsr3_static(int32_t n, const int32_t* rowptr, const int32_t* co
                              const float* vals, const float* b, double tol, int32_t maxit,
                              float* dv, int32_t* iterations, double* rel_residual,
                              void* stream);
+
+/* Self-test of the device-side bounded waits that keep every kernel of this
+ * library from hanging.  which = 0 runs the SpMV pipeline's mbarrier wait on
+ * a barrier phase that gets no arrival; which = 1 runs the PCG grid
+ * barrier's counter poll on a counter that gets one arrival of the two it
+ * waits for.  Each waits limit_seconds (0 < limit_seconds <= 10; the
+ * library's own waits use 2 s) on the current device's legacy stream, gives
+ * up and records the timeout in a device status word, which is copied to
+ * *status (if not NULL; bit 4 = a wait gave up).  Returns PCLOTH_ERR_CUDA
+ * with the message "device wait timed out" -- exactly what a real timeout
+ * reports -- when the wait gave up as designed, PCLOTH_OK if it did not,
+ * PCLOTH_ERR_INVALID_ARG for a bad argument.  Allocates 64 bytes of device
+ * memory for the call and synchronises the device.  The GPU context stays
+ * usable afterwards.  Errors are described by pcloth_last_error(NULL). */
+int pcloth_selftest_bounded_wait(int which, double limit_seconds, uint32_t* status);
 
 /* Free every buffer of the handle (synchronises its stream first). */
 void pcloth_destroy(pcloth_t h);

@@ -89,6 +89,17 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
+// Polls the counter until it reaches `target`; false once `limit_ns` has
+// passed.
+__device__ __forceinline__ bool poll_bounded(const unsigned long long* counter,
+                                             unsigned long long target, uint64_t limit_ns) {
+  if (ld_acquire(counter) >= target) return true;
+  const uint64_t t0 = now_ns();
+  while (ld_acquire(counter) < target)
+    if (now_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
 // Grid-wide barrier.  Every CTA adds 1 to the counter (zeroed before the
 // launch) once per barrier, so the b-th barrier is complete when the counter
 // reaches b * gridDim.x.  The fences make each CTA's writes before the
@@ -104,16 +115,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned l
     const unsigned long long target = epoch * gridDim.x;
     __threadfence();
     atomicAdd(bar, 1ull);
-    bool ok = true;
-    if (ld_acquire(bar) < target) {
-      const uint64_t t0 = now_ns();
-      while (ld_acquire(bar) < target) {
-        if (now_ns() - t0 > kWaitNs) {
-          ok = false;
-          break;
-        }
-      }
-    }
+    const bool ok = poll_bounded(bar, target, kWaitNs);
     __threadfence();
     *ok_sh = ok && !(ld_acquire(status) & ST_WAIT_TIMEOUT);
   }
@@ -524,7 +526,54 @@ cudaError_t launch_loop(const LoopArgs& a, int grid, cudaStream_t stream) {
                                      dim3(kPipeThreads), params, Pipe<BW>::kSmem, stream);
 }
 
+// Self-tests of the bounded waits: each kernel waits, with a short limit, on
+// something nothing will ever complete -- an mbarrier phase that gets no
+// arrival, or a barrier counter that gets one arrival of the two it waits
+// for -- and must return with ST_WAIT_TIMEOUT set instead of hanging.
+__global__ void selftest_mbarrier(uint64_t limit_ns, uint32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !wait_bounded(&bar, 0u, limit_ns)) atomicOr(status, ST_WAIT_TIMEOUT);
+}
+
+__global__ void selftest_counter(unsigned long long* counter, uint64_t limit_ns,
+                                 uint32_t* status) {
+  if (threadIdx.x == 0) {
+    atomicAdd(counter, 1ull);
+    if (!poll_bounded(counter, 2ull, limit_ns)) atomicOr(status, ST_WAIT_TIMEOUT);
+  }
+}
+
 }  // namespace
+
+int selftest_bounded_wait(int which, double limit_s, uint32_t* status_out) {
+  unsigned char* buf = nullptr;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&buf), 64);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "self-test buffer");
+  uint32_t* status = reinterpret_cast<uint32_t*>(buf);
+  unsigned long long* counter = reinterpret_cast<unsigned long long*>(buf + 16);
+  e = cudaMemset(buf, 0, 64);
+  const uint64_t limit_ns = uint64_t(limit_s * 1e9);
+  if (e == cudaSuccess) {
+    if (which == 0)
+      selftest_mbarrier<<<1, 32>>>(limit_ns, status);
+    else
+      selftest_counter<<<1, 32>>>(counter, limit_ns, status);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  uint32_t st = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&st, status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  cudaFree(buf);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "self-test wait");
+  if (status_out) *status_out = st;
+  if (st & ST_WAIT_TIMEOUT) return fail(nullptr, PCLOTH_ERR_CUDA, "device wait timed out");
+  return PCLOTH_OK;
+}
 
 int pcg_loop_grid(int blk, int32_t n, int device, int sm_count, int* grid) {
   return blk == kSymBlock ? loop_grid_for<kSymBlock>(n, device, sm_count, grid)

@@ -206,6 +206,7 @@ int launch_vals_expand(Handle* h, float* out9, int64_t nnzb);
 // CTAs of the persistent PCG kernel for blocks of blk floats: the streaming
 // grid, capped at what can be co-resident (a cooperative launch needs all).
 int pcg_loop_grid(int blk, int32_t n, int device, int sm_count, int* grid);
+int selftest_bounded_wait(int which, double limit_s, uint32_t* status_out);
 int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv,
               int32_t* iterations, double* rel_residual);
 int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt);

@@ -114,13 +114,14 @@ __device__ __forceinline__ uint64_t now_ns() {
 }
 
 // Wait with a wall-clock bound; false when the bound is hit.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
+                                             uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = now_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (now_ns() - t0 > kWaitNs) return false;
+    if (now_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -31,7 +31,7 @@ EXPORTS = ("pcloth_create", "pcloth_assemble", "pcloth_spmv", "pcloth_solve", "p
            "pcloth_step_host", "pcloth_nnzb", "pcloth_export", "pcloth_set_stream",
            "pcloth_sync", "pcloth_last_error", "pcloth_destroy", "pcloth_profile_enable",
            "pcloth_profile_read", "pcloth_solve_bsr3_static", "pcloth_bell_build",
-           "pcloth_spmv_bell", "pcloth_find_contacts")
+           "pcloth_spmv_bell", "pcloth_find_contacts", "pcloth_selftest_bounded_wait")
 
 STATIC_MAX_VERTS = 16384   # PCLOTH_STATIC_MAX_VERTS
 
@@ -96,6 +96,7 @@ def lib():
         L.pcloth_profile_read.argtypes = [vp, P(dbl), P(i64), ctypes.c_int]
         L.pcloth_solve_bsr3_static.argtypes = [i32, vp, vp, vp, vp, dbl, i32, vp, P(i32), P(dbl),
                                                vp]
+        L.pcloth_selftest_bounded_wait.argtypes = [ctypes.c_int, dbl, P(ctypes.c_uint32)]
         for name in EXPORTS:
             f = getattr(L, name)
             if name not in ("pcloth_last_error", "pcloth_destroy"):
@@ -340,6 +341,18 @@ def pcloth_solve_bsr3_static(n: int, rowptr, colind, vals, b, tol: float, maxit:
     if rc not in (OK, NOT_CONVERGED):
         _raise(None, rc)
     return int(it.value), float(rr.value), rc
+
+
+def pcloth_selftest_bounded_wait(which: int, limit_seconds: float):
+    """Runs one of the library's bounded device waits on something that never
+    completes (which = 0: the SpMV pipeline's mbarrier wait; 1: the PCG grid
+    barrier's counter poll) with a limit of limit_seconds.  Returns (code,
+    status word, message): a wait that gave up as designed returns ERR_CUDA,
+    the device status word with bit 4 set and "device wait timed out"."""
+    st = ctypes.c_uint32(0)
+    rc = lib().pcloth_selftest_bounded_wait(int(which), float(limit_seconds), ctypes.byref(st))
+    msg = lib().pcloth_last_error(None)
+    return rc, int(st.value), (msg.decode() if msg else "")
 
 
 # ------------------------------------------------------------ convenience --
