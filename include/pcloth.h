@@ -249,15 +249,20 @@ int pcloth_solve_bsr3_static(int32_t n, const int32_t* rowptr, const int32_t* co
  * library from hanging.  which = 0 runs the SpMV pipeline's mbarrier wait on
  * a barrier phase that gets no arrival; which = 1 runs the PCG grid
  * barrier's counter poll on a counter that gets one arrival of the two it
- * waits for.  Each waits limit_seconds (0 < limit_seconds <= 10; the
- * library's own waits use 2 s) on the current device's legacy stream, gives
- * up and records the timeout in a device status word, which is copied to
- * *status (if not NULL; bit 4 = a wait gave up).  Returns PCLOTH_ERR_CUDA
- * with the message "device wait timed out" -- exactly what a real timeout
- * reports -- when the wait gave up as designed, PCLOTH_OK if it did not,
- * PCLOTH_ERR_INVALID_ARG for a bad argument.  Allocates 64 bytes of device
- * memory for the call and synchronises the device.  The GPU context stays
- * usable afterwards.  Errors are described by pcloth_last_error(NULL). */
+ * waits for; both wait limit_seconds (0 < limit_seconds <= 10; the
+ * library's own waits use 2 s), give up and record the timeout.  which = 2
+ * runs the PCG grid barrier itself in one cooperative launch of two CTAs,
+ * one of which arrives marked as having timed out (its arrival carries the
+ * mark, as after a real timeout): both CTAs must leave the barrier with the
+ * timeout verdict at once.  The device status word is copied to *status (if
+ * not NULL): bit 4 = a wait gave up; for which = 2, bits 8-15 = how many of
+ * the two CTAs left the barrier with the verdict.  Runs on the current
+ * device's legacy stream.  Returns PCLOTH_ERR_CUDA with the message "device
+ * wait timed out" -- what a real timeout reports -- when the timeout was
+ * recorded as designed, PCLOTH_OK if it was not, PCLOTH_ERR_INVALID_ARG for
+ * a bad argument.  Allocates 64 bytes of device memory for the call and
+ * synchronises the device; the GPU context stays usable afterwards.  Errors
+ * are described by pcloth_last_error(NULL). */
 int pcloth_selftest_bounded_wait(int which, double limit_seconds, uint32_t* status);
 
 /* Free every buffer of the handle (synchronises its stream first). */

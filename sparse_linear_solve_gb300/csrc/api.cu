@@ -493,7 +493,7 @@ void pcloth_destroy(pcloth_t ht) { free_handle(reinterpret_cast<Handle*>(ht)); }
 
 int pcloth_selftest_bounded_wait(int which, double limit_seconds, uint32_t* status) {
   g_create_err.clear();
-  if (which != 0 && which != 1) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "which must be 0 or 1");
+  if (which < 0 || which > 2) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "which must be 0, 1 or 2");
   if (!(limit_seconds > 0.0) || !(limit_seconds <= 10.0))
     return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "limit_seconds must be in (0, 10]");
   return selftest_bounded_wait(which, limit_seconds, status);

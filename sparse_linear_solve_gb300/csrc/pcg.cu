@@ -83,44 +83,59 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
   return v;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
+// A CTA in which a wait timed out adds kPoison to the barrier counter with
+// its next arrival, so that every CTA sees the timeout in the value that
+// completes its own wait: the arrivals are counted in the bits below.
+constexpr unsigned long long kPoison = 1ull << 40;
 
-// Polls the counter until it reaches `target`; false once `limit_ns` has
-// passed.
+// Polls the counter until its arrival count reaches `target`; false once
+// `limit_ns` has passed.  *seen: the last value read.
 __device__ __forceinline__ bool poll_bounded(const unsigned long long* counter,
-                                             unsigned long long target, uint64_t limit_ns) {
-  if (ld_acquire(counter) >= target) return true;
-  const uint64_t t0 = now_ns();
-  while (ld_acquire(counter) < target)
-    if (now_ns() - t0 > limit_ns) return false;
+                                             unsigned long long target, uint64_t limit_ns,
+                                             unsigned long long* seen) {
+  unsigned long long v = ld_acquire(counter);
+  if ((v & (kPoison - 1)) < target) {
+    const uint64_t t0 = now_ns();
+    while (((v = ld_acquire(counter)) & (kPoison - 1)) < target)
+      if (now_ns() - t0 > limit_ns) {
+        *seen = v;
+        return false;
+      }
+  }
+  *seen = v;
   return true;
 }
 
 // Grid-wide barrier.  Every CTA adds 1 to the counter (zeroed before the
-// launch) once per barrier, so the b-th barrier is complete when the counter
-// reaches b * gridDim.x.  The fences make each CTA's writes before the
-// barrier visible to every CTA after it (the release/acquire pattern of a
-// cooperative-groups grid sync).  Returns false, the same in every thread of
-// the CTA, if the wait ran past kWaitNs or any thread of the grid has
-// recorded a timeout: the caller then leaves its loop.
+// launch) once per barrier, so the b-th barrier is complete when the
+// arrivals reach b * gridDim.x.  Thread 0 arrives with a release add and
+// waits with acquire loads, and the CTA barriers on both sides carry the
+// ordering to its other threads: each CTA's writes before the barrier are
+// visible to every CTA after it.  Returns false, the same in every thread of
+// the CTA, if the wait ran past kWaitNs or any CTA of the grid arrived
+// poisoned (fail_sh set: one of its waits timed out); the caller then
+// leaves its loop.
 __device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned long long& epoch,
-                                             const uint32_t* status, int* ok_sh) {
+                                             const int* fail_sh, int* ok_sh) {
   __syncthreads();
   if (threadIdx.x == 0) {
     ++epoch;
     const unsigned long long target = epoch * gridDim.x;
-    __threadfence();
-    atomicAdd(bar, 1ull);
-    const bool ok = poll_bounded(bar, target, kWaitNs);
-    __threadfence();
-    *ok_sh = ok && !(ld_acquire(status) & ST_WAIT_TIMEOUT);
+    const unsigned long long inc = 1ull + (*fail_sh ? kPoison : 0ull);
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(bar), "l"(inc) : "memory");
+    unsigned long long v = 0;
+    const bool ok = poll_bounded(bar, target, kWaitNs, &v);
+    *ok_sh = ok && v < kPoison;
   }
   __syncthreads();
   return *ok_sh != 0;
+}
+
+// Records a wait that gave up: in the status word for the host, and in the
+// CTA's flag, which poisons its next barrier arrival.
+__device__ __forceinline__ void timed_out(uint32_t* status, int* fail_sh) {
+  atomicOr(status, ST_WAIT_TIMEOUT);
+  *fail_sh = 1;
 }
 
 constexpr int kTileCache = 256;   // tiles per CTA whose block ranges stay in shared memory
@@ -191,6 +206,7 @@ pcg_loop(LoopArgs a) {
   const PipeShared sh = pipe_shared<BW>(smem);
   __shared__ float2 red_sh[33 * 2];
   __shared__ int ok_sh;
+  __shared__ int fail_sh;   // a wait of this CTA timed out
   __shared__ int stop_sh;
   __shared__ float scal_sh;
   __shared__ Lead L;
@@ -211,6 +227,7 @@ pcg_loop(LoopArgs a) {
   const bool timer = a.phase_ns != nullptr && blockIdx.x == 0 && tid == 0;
   Consumer C;
   if (tid == 0) {
+    fail_sh = 0;
     producer_begin(L.P, m);
     L.epoch = L.t_s = L.t_u = L.t_p = L.n_timed = L.t_prev = 0;
   }
@@ -239,7 +256,7 @@ pcg_loop(LoopArgs a) {
       my_rec[REC_BB] = df_pack(v[1]);
     }
   }
-  bool run = grid_barrier(a.bar, L.epoch, a.status, &ok_sh);
+  bool run = grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh);
 
   if (run) {
     Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
@@ -269,7 +286,7 @@ pcg_loop(LoopArgs a) {
       if (!stop) {
         Producer P = L.P;
         for (int j = 0; j < kPipeStages && !P.ended; ++j)
-          if (producer_step<BW>(P, sh, m) < 0) atomicOr(a.status, ST_WAIT_TIMEOUT);
+          if (producer_step<BW>(P, sh, m) < 0) timed_out(a.status, &fail_sh);
         L.P = P;
       }
     }
@@ -284,14 +301,14 @@ pcg_loop(LoopArgs a) {
     if (tid < 32) {
       if (tid == 0) {
         Producer P = L.P;
-        if (!producer_pass<BW>(P, sh, m)) atomicOr(a.status, ST_WAIT_TIMEOUT);
+        if (!producer_pass<BW>(P, sh, m)) timed_out(a.status, &fail_sh);
         L.P = P;
       }
     } else {
       const Vec vm = vec_access();
       PGather g{a.p, vm};
       PEpi e{a.p, a.q, a.vs, vm, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
-      if (!consumer_pass<BW>(C, sh, g, e)) atomicOr(a.status, ST_WAIT_TIMEOUT);
+      if (!consumer_pass<BW>(C, sh, g, e)) timed_out(a.status, &fail_sh);
       pq = e.pq;
     }
     {
@@ -299,7 +316,7 @@ pcg_loop(LoopArgs a) {
       block_sum_df<kPipeThreads, 1>(t, red_sh);
       if (tid == 0) my_rec[REC_PQ] = df_pack(t[0]);
     }
-    if (!grid_barrier(a.bar, L.epoch, a.status, &ok_sh)) break;
+    if (!grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh)) break;
     if (timer) {
       const unsigned long long t = now_ns();
       L.t_s += t - L.t_prev;
@@ -379,7 +396,7 @@ pcg_loop(LoopArgs a) {
         my_rec[REC_RR] = df_pack(o[1]);
       }
     }
-    if (!grid_barrier(a.bar, L.epoch, a.status, &ok_sh)) break;
+    if (!grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh)) break;
     if (timer) {
       const unsigned long long t = now_ns();
       L.t_u += t - L.t_prev;
@@ -442,7 +459,7 @@ pcg_loop(LoopArgs a) {
       }
     }
     if (stop) break;
-    if (!grid_barrier(a.bar, L.epoch, a.status, &ok_sh)) break;
+    if (!grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh)) break;
     if (timer) {
       const unsigned long long t = now_ns();
       L.t_p += t - L.t_prev;
@@ -540,11 +557,25 @@ __global__ void selftest_mbarrier(uint64_t limit_ns, uint32_t* status) {
   if (threadIdx.x == 0 && !wait_bounded(&bar, 0u, limit_ns)) atomicOr(status, ST_WAIT_TIMEOUT);
 }
 
+// Two CTAs of one cooperative launch meet at the PCG kernel's grid barrier;
+// CTA 1 arrives poisoned, as after a timeout.  Both must leave the barrier
+// with the timeout verdict (each adds 1 to `seen`) instead of going on.
+__global__ void selftest_poison(unsigned long long* bar, unsigned int* seen, uint32_t* status) {
+  __shared__ int fail_sh, ok_sh;
+  unsigned long long epoch = 0;
+  if (threadIdx.x == 0) fail_sh = blockIdx.x == 1 ? 1 : 0;
+  if (!grid_barrier(bar, epoch, &fail_sh, &ok_sh) && threadIdx.x == 0) {
+    atomicOr(status, ST_WAIT_TIMEOUT);
+    atomicAdd(seen, 1u);
+  }
+}
+
 __global__ void selftest_counter(unsigned long long* counter, uint64_t limit_ns,
                                  uint32_t* status) {
   if (threadIdx.x == 0) {
     atomicAdd(counter, 1ull);
-    if (!poll_bounded(counter, 2ull, limit_ns)) atomicOr(status, ST_WAIT_TIMEOUT);
+    unsigned long long v = 0;
+    if (!poll_bounded(counter, 2ull, limit_ns, &v)) atomicOr(status, ST_WAIT_TIMEOUT);
   }
 }
 
@@ -555,22 +586,30 @@ int selftest_bounded_wait(int which, double limit_s, uint32_t* status_out) {
   cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&buf), 64);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "self-test buffer");
   uint32_t* status = reinterpret_cast<uint32_t*>(buf);
+  unsigned int* seen = reinterpret_cast<unsigned int*>(buf + 4);
   unsigned long long* counter = reinterpret_cast<unsigned long long*>(buf + 16);
   e = cudaMemset(buf, 0, 64);
   const uint64_t limit_ns = uint64_t(limit_s * 1e9);
   if (e == cudaSuccess) {
-    if (which == 0)
+    if (which == 0) {
       selftest_mbarrier<<<1, 32>>>(limit_ns, status);
-    else
+      e = cudaGetLastError();
+    } else if (which == 1) {
       selftest_counter<<<1, 32>>>(counter, limit_ns, status);
-    e = cudaGetLastError();
+      e = cudaGetLastError();
+    } else {
+      void* args[] = {&counter, &seen, &status};
+      e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(selftest_poison), dim3(2),
+                                      dim3(32), args, 0, nullptr);
+    }
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  uint32_t st = 0;
+  uint32_t st = 0, sn = 0;
   if (e == cudaSuccess) e = cudaMemcpy(&st, status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&sn, seen, sizeof(uint32_t), cudaMemcpyDeviceToHost);
   cudaFree(buf);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "self-test wait");
-  if (status_out) *status_out = st;
+  if (status_out) *status_out = st | (sn << 8);
   if (st & ST_WAIT_TIMEOUT) return fail(nullptr, PCLOTH_ERR_CUDA, "device wait timed out");
   return PCLOTH_OK;
 }

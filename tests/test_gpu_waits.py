@@ -44,7 +44,19 @@ def test_bounded_wait_gives_up_and_reports(which):
     assert np.isfinite(dv.cpu().numpy()).all()
 
 
+def test_poisoned_grid_barrier_stops_every_cta():
+    """One CTA of two arrives at the PCG kernel's grid barrier marked as
+    having timed out; both leave at once with the timeout verdict."""
+    t0 = time.perf_counter()
+    rc, status, msg = pc.pcloth_selftest_bounded_wait(2, 1.0)
+    elapsed = time.perf_counter() - t0
+    assert rc == pc.ERR_CUDA and "timed out" in msg
+    assert status & WAIT_TIMEOUT_BIT
+    assert (status >> 8) & 0xFF == 2
+    assert elapsed < 1.5          # no CTA waited for the 2 s limit
+
+
 def test_selftest_rejects_bad_arguments():
-    for which, limit in ((2, 0.05), (0, 0.0), (1, 11.0)):
+    for which, limit in ((3, 0.05), (-1, 0.05), (0, 0.0), (1, 11.0)):
         rc, _, _ = pc.pcloth_selftest_bounded_wait(which, limit)
         assert rc == pc.ERR_INVALID_ARG
