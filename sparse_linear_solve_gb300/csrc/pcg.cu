@@ -250,7 +250,7 @@ pcg_loop(LoopArgs a) {
       bb += dot3(bv, bv);
     }
     Dfloat v[2] = {df_of(rz), df_of(bb)};
-    block_sum_df<kPipeThreads, 2>(v, red_sh);
+    block_sum_df0<kPipeThreads, 2>(v, red_sh);
     if (tid == 0) {
       my_rec[REC_RZ] = df_pack(v[0]);
       my_rec[REC_BB] = df_pack(v[1]);
@@ -261,7 +261,7 @@ pcg_loop(LoopArgs a) {
   if (run) {
     Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
                    records_share(a.rec, gridDim.x, REC_BB, kPipeThreads)};
-    block_sum_df<kPipeThreads, 2>(v, red_sh);
+    block_sum_df0<kPipeThreads, 2>(v, red_sh);
     if (tid == 0) {
       const double bbd = df_value(v[1]);
       L.rz_old = df_value(v[0]);
@@ -313,7 +313,7 @@ pcg_loop(LoopArgs a) {
     }
     {
       Dfloat t[1] = {df_of(pq)};
-      block_sum_df<kPipeThreads, 1>(t, red_sh);
+      block_sum_df0<kPipeThreads, 1>(t, red_sh);
       if (tid == 0) my_rec[REC_PQ] = df_pack(t[0]);
     }
     if (!grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh)) break;
@@ -336,7 +336,7 @@ pcg_loop(LoopArgs a) {
     }
     {
       Dfloat v[1] = {records_share(a.rec, gridDim.x, REC_PQ, kPipeThreads)};
-      block_sum_df<kPipeThreads, 1>(v, red_sh);
+      block_sum_df0<kPipeThreads, 1>(v, red_sh);
       if (tid == 0) {
         const double pqd = df_value(v[0]), rz_old = L.rz_old, bbd = L.bbd;
         int stop = 0;
@@ -390,7 +390,7 @@ pcg_loop(LoopArgs a) {
         }
       }
       Dfloat o[2] = {df_of(arz), df_of(arr)};
-      block_sum_df<kPipeThreads, 2>(o, red_sh);
+      block_sum_df0<kPipeThreads, 2>(o, red_sh);
       if (tid == 0) {
         my_rec[REC_RZ] = df_pack(o[0]);
         my_rec[REC_RR] = df_pack(o[1]);
@@ -407,7 +407,7 @@ pcg_loop(LoopArgs a) {
     {
       Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
                      records_share(a.rec, gridDim.x, REC_RR, kPipeThreads)};
-      block_sum_df<kPipeThreads, 2>(v, red_sh);
+      block_sum_df0<kPipeThreads, 2>(v, red_sh);
       if (tid == 0) {
         const double rz = df_value(v[0]), rr = df_value(v[1]);
         const double rz_old = L.rz_old, bbd = L.bbd;

@@ -242,11 +242,12 @@ __device__ __forceinline__ Dfloat df_of(float2 x) { return Dfloat{x.x, x.y}; }
 __device__ __forceinline__ float2 df_pack(Dfloat x) { return make_float2(x.hi, x.lo); }
 __device__ __forceinline__ double df_value(Dfloat x) { return double(x.hi) + double(x.lo); }
 
-// Block-wide sums of N double-floats per thread: a shuffle tree per warp,
-// then warp 0 adds the warp totals in order; results are broadcast to every
-// thread.  sh must hold 33 * N float2.
+// Block-wide sums of N double-floats per thread, for thread 0 only: a
+// shuffle tree per warp, then lane q of warp 0 adds the warp totals of value
+// q in order and hands it to lane 0.  The result is valid in thread 0; the
+// caller synchronises the block again before sh is reused.
 template <int THREADS, int N>
-__device__ __forceinline__ void block_sum_df(Dfloat (&v)[N], float2* sh) {
+__device__ __forceinline__ void block_sum_df0(Dfloat (&v)[N], float2* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int q = 0; q < N; ++q) {
@@ -259,15 +260,16 @@ __device__ __forceinline__ void block_sum_df(Dfloat (&v)[N], float2* sh) {
     if (lane == 0) sh[q * 32 + warp] = df_pack(v[q]);
   }
   __syncthreads();
-  if (warp == 0 && lane < N) {
-    Dfloat t = df_of(sh[lane * 32]);
-    for (int w = 1; w < THREADS / 32; ++w) t = df_add(t, df_of(sh[lane * 32 + w]));
-    sh[32 * N + lane] = df_pack(t);
-  }
-  __syncthreads();
+  if (warp == 0) {
+    Dfloat t{0.f, 0.f};
+    if (lane < N) {
+      t = df_of(sh[lane * 32]);
+      for (int w = 1; w < THREADS / 32; ++w) t = df_add(t, df_of(sh[lane * 32 + w]));
+    }
 #pragma unroll
-  for (int q = 0; q < N; ++q) v[q] = df_of(sh[32 * N + q]);
-  __syncthreads();
+    for (int q = 0; q < N; ++q)
+      v[q] = Dfloat{__shfl_sync(0xffffffffu, t.hi, q), __shfl_sync(0xffffffffu, t.lo, q)};
+  }
 }
 
 // Adds slot `slot` of `count` partial records (kRecSlots float2 each) that
