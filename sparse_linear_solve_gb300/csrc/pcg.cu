@@ -349,7 +349,9 @@ pcg_loop(LoopArgs a) {
             atomicOr(a.status, fin ? ST_BREAKDOWN : ST_NONFINITE);
           }
         }
-        scal_sh = float(rz_old / pqd);
+        // alpha in fp32 from the fp64-rounded sums: the vectors are updated
+        // in fp32 anyway, and an fp64 division is a slow path on this GPU
+        scal_sh = float(rz_old) / float(pqd);
         stop_sh = stop;
       }
       __syncthreads();
@@ -428,7 +430,7 @@ pcg_loop(LoopArgs a) {
         }
         if (stop && blockIdx.x == 0)
           *a.state = PcgState{1, k + 1, code, 0, sqrt(rr / bbd), sqrt(bbd)};
-        scal_sh = float(rz / rz_old);
+        scal_sh = float(rz) / float(rz_old);   // beta, likewise in fp32
         stop_sh = stop;
         L.rr_last = rr;
         L.rz_old = rz;
