@@ -27,8 +27,9 @@
 // compete with them.
 //
 // Every wait (mbarrier, grid barrier) is bounded in time: on a timeout the
-// kernel records ST_WAIT_TIMEOUT, waits (bounded) for its own copies in
-// flight and returns; the host reports an error.
+// CTA records ST_WAIT_TIMEOUT and marks its next barrier arrival, so that
+// every CTA leaves the loop at that barrier; each then waits (bounded) for
+// its own copies in flight and returns, and the host reports an error.
 
 #include <algorithm>
 
