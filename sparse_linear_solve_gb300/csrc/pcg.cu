@@ -116,20 +116,35 @@ __device__ __forceinline__ bool poll_bounded(const unsigned long long* counter,
 // the CTA, if the wait ran past kWaitNs or any CTA of the grid arrived
 // poisoned (fail_sh set: one of its waits timed out); the caller then
 // leaves its loop.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned long long& epoch,
-                                             const int* fail_sh, int* ok_sh) {
+//
+// The barrier comes in two halves, so that a CTA can load its own rows for
+// the next phase between its arrival and its wait (grid_arrive, then
+// grid_wait; grid_barrier is both).  epoch is thread 0's.
+__device__ __forceinline__ void grid_arrive(unsigned long long* bar, unsigned long long& epoch,
+                                            const int* fail_sh) {
   __syncthreads();
   if (threadIdx.x == 0) {
     ++epoch;
-    const unsigned long long target = epoch * gridDim.x;
     const unsigned long long inc = 1ull + (*fail_sh ? kPoison : 0ull);
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(bar), "l"(inc) : "memory");
+  }
+}
+
+__device__ __forceinline__ bool grid_wait(const unsigned long long* bar,
+                                          const unsigned long long& epoch, int* ok_sh) {
+  if (threadIdx.x == 0) {
     unsigned long long v = 0;
-    const bool ok = poll_bounded(bar, target, kWaitNs, &v);
+    const bool ok = poll_bounded(bar, epoch * gridDim.x, kWaitNs, &v);
     *ok_sh = ok && v < kPoison;
   }
   __syncthreads();
   return *ok_sh != 0;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned long long& epoch,
+                                             const int* fail_sh, int* ok_sh) {
+  grid_arrive(bar, epoch, fail_sh);
+  return grid_wait(bar, epoch, ok_sh);
 }
 
 // Records a wait that gave up: in the status word for the host, and in the
@@ -317,16 +332,9 @@ pcg_loop(LoopArgs a) {
       block_sum_df0<kPipeThreads, 1>(t, red_sh);
       if (tid == 0) my_rec[REC_PQ] = df_pack(t[0]);
     }
-    if (!grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh)) break;
-    if (timer) {
-      const unsigned long long t = now_ns();
-      L.t_s += t - L.t_prev;
-      L.t_prev = t;
-      ++L.n_timed;
-    }
-
-    // ---- U: alpha; r, z; partials r.z, r.r ----------------------------------
-    // the first row's inputs do not depend on alpha: load them under the reduction
+    grid_arrive(a.bar, L.epoch, &fail_sh);
+    // The update's first row: its inputs are this CTA's own rows and do not
+    // depend on alpha, so they load while the other CTAs arrive.
     const int32_t i_first = tid < nslots ? own_row(tid) : n;
     float3 q_first = make_float3(0.f, 0.f, 0.f), r_first = q_first;
     Sym3 p_first{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -335,6 +343,15 @@ pcg_loop(LoopArgs a) {
       r_first = ld3(a.r, a.vs, i_first);
       p_first = ld_sym(a.pinv, a.vs, i_first);
     }
+    if (!grid_wait(a.bar, L.epoch, &ok_sh)) break;
+    if (timer) {
+      const unsigned long long t = now_ns();
+      L.t_s += t - L.t_prev;
+      L.t_prev = t;
+      ++L.n_timed;
+    }
+
+    // ---- U: alpha; r, z; partials r.z, r.r ----------------------------------
     {
       Dfloat v[1] = {records_share(a.rec, gridDim.x, REC_PQ, kPipeThreads)};
       block_sum_df0<kPipeThreads, 1>(v, red_sh);
@@ -399,7 +416,17 @@ pcg_loop(LoopArgs a) {
         my_rec[REC_RR] = df_pack(o[1]);
       }
     }
-    if (!grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh)) break;
+    grid_arrive(a.bar, L.epoch, &fail_sh);
+    // the direction phase's first row (the update's first row: this thread
+    // wrote its z), loaded while the other CTAs arrive
+    float4 pv_first = make_float4(0.f, 0.f, 0.f, 0.f);
+    float3 dv_first = make_float3(0.f, 0.f, 0.f), z_first = dv_first;
+    if (i_first < n) {
+      pv_first = a.p[i_first];
+      dv_first = ld3(a.dv, a.vs, i_first);
+      z_first = ld3(a.z, a.vs, i_first);
+    }
+    if (!grid_wait(a.bar, L.epoch, &ok_sh)) break;
     if (timer) {
       const unsigned long long t = now_ns();
       L.t_u += t - L.t_prev;
@@ -447,8 +474,17 @@ pcg_loop(LoopArgs a) {
       float* __restrict__ dv_ = a.dv;
       const float* __restrict__ zv_ = a.z;
       const int64_t vs = a.vs;
+      if (i_first < n) {
+        const float4 pv = pv_first;
+        st3(dv_, vs, i_first,
+            make_float3(fmaf(alpha, pv.x, dv_first.x), fmaf(alpha, pv.y, dv_first.y),
+                        fmaf(alpha, pv.z, dv_first.z)));
+        if (!stop)
+          pv_[i_first] = make_float4(fmaf(beta, pv.x, z_first.x), fmaf(beta, pv.y, z_first.y),
+                                     fmaf(beta, pv.z, z_first.z), 0.f);
+      }
 #pragma unroll 2
-      for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+      for (int32_t f = tid + kPipeThreads; f < nslots; f += kPipeThreads) {
         const int32_t i = own_row(f);
         if (i >= n) break;
         const float4 pv = pv_[i];
