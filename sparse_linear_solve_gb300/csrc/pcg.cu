@@ -275,8 +275,11 @@ pcg_loop(LoopArgs a) {
   bool run = grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh);
 
   if (run) {
-    Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
-                   records_share(a.rec, gridDim.x, REC_BB, kPipeThreads)};
+    Dfloat v[2], rz[1], bb[1];
+    records_share<1>(a.rec, gridDim.x, REC_RZ, kPipeThreads, rz);
+    records_share<1>(a.rec, gridDim.x, REC_BB, kPipeThreads, bb);
+    v[0] = rz[0];
+    v[1] = bb[0];
     block_sum_df0<kPipeThreads, 2>(v, red_sh);
     if (tid == 0) {
       const double bbd = df_value(v[1]);
@@ -353,7 +356,8 @@ pcg_loop(LoopArgs a) {
 
     // ---- U: alpha; r, z; partials r.z, r.r ----------------------------------
     {
-      Dfloat v[1] = {records_share(a.rec, gridDim.x, REC_PQ, kPipeThreads)};
+      Dfloat v[1];
+      records_share<1>(a.rec, gridDim.x, REC_PQ, kPipeThreads, v);
       block_sum_df0<kPipeThreads, 1>(v, red_sh);
       if (tid == 0) {
         const double pqd = df_value(v[0]), rz_old = L.rz_old, bbd = L.bbd;
@@ -435,8 +439,9 @@ pcg_loop(LoopArgs a) {
 
     // ---- P: convergence, beta; dv += alpha p, p = z + beta p ------------------
     {
-      Dfloat v[2] = {records_share(a.rec, gridDim.x, REC_RZ, kPipeThreads),
-                     records_share(a.rec, gridDim.x, REC_RR, kPipeThreads)};
+      static_assert(REC_RR == REC_RZ + 1 && REC_RZ % 2 == 0, "r.z, r.r: one 16-byte load");
+      Dfloat v[2];
+      records_share<2>(a.rec, gridDim.x, REC_RZ, kPipeThreads, v);
       block_sum_df0<kPipeThreads, 2>(v, red_sh);
       if (tid == 0) {
         const double rz = df_value(v[0]), rr = df_value(v[1]);
@@ -749,6 +754,8 @@ constexpr int64_t kStaticPlane =                                          // flo
     (int64_t(PCLOTH_STATIC_MAX_VERTS) + 31) / 32 * 32 + 64;
 constexpr int kStaticPlanes = 6 + 4 * 3;   // P; dv, r, z, q
 constexpr int kStaticMaxRecords = 2048;    // CTAs of the solve
+static_assert((sizeof(float4) * kStaticVec + sizeof(float) * kStaticPlanes * kStaticPlane) % 16 ==
+                  0, "the partial-sum records start 16-byte aligned");
 constexpr size_t kStaticBytes = sizeof(float4) * size_t(kStaticVec) +
                                 sizeof(float) * size_t(kStaticPlanes) * size_t(kStaticPlane) +
                                 sizeof(float2) * size_t(kRecSlots) * size_t(kStaticMaxRecords) +

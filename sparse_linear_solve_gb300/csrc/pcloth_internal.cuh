@@ -53,7 +53,8 @@ constexpr int kVecThreads = 256;
 // Per-CTA partial sums of the PCG dot products, one double-float (float2)
 // per slot: p.q, r.z, r.r, b.b.
 constexpr int kRecSlots = 4;
-enum { REC_PQ = 0, REC_RZ = 1, REC_RR = 2, REC_BB = 3 };
+// r.z and r.r share a 16-byte half of the record: one load reads both
+enum { REC_PQ = 0, REC_BB = 1, REC_RZ = 2, REC_RR = 3 };
 
 // --------------------------------------------------------------- handle ----
 struct Profile {
@@ -272,15 +273,41 @@ __device__ __forceinline__ void block_sum_df0(Dfloat (&v)[N], float2* sh) {
   }
 }
 
-// Adds slot `slot` of `count` partial records (kRecSlots float2 each) that
-// the CTAs of the grid wrote, this thread's share in index order.  The loads
-// bypass L1: other SMs wrote the records.
-__device__ __forceinline__ Dfloat records_share(const float2* rec, int count, int slot,
-                                                int threads) {
-  Dfloat a{0.f, 0.f};
-  for (int t = threadIdx.x; t < count; t += threads)
-    a = df_add(a, df_of(__ldcg(&rec[t * kRecSlots + slot])));
-  return a;
+// Adds slots slot0 .. slot0 + N - 1 of `count` partial records (kRecSlots
+// float2 each) that the CTAs of the grid wrote: this thread's share, records
+// threadIdx.x, + threads, ..., in index order.  The loads bypass L1 (other
+// SMs wrote the records) and are issued two records at a time before they
+// are added, so that their latencies overlap; with N = 2 (slot0 even) a
+// record's two slots are one 16-byte load.
+template <int N>
+__device__ __forceinline__ void records_share(const float2* rec, int count, int slot0,
+                                              int threads, Dfloat (&a)[N]) {
+  static_assert(N == 1 || N == 2, "one or two slots");
+#pragma unroll
+  for (int q = 0; q < N; ++q) a[q] = Dfloat{0.f, 0.f};
+  auto load = [&](int t, float2(&x)[N]) {
+    if constexpr (N == 2) {
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(rec + t * kRecSlots + slot0));
+      x[0] = make_float2(w.x, w.y);
+      x[1] = make_float2(w.z, w.w);
+    } else {
+      x[0] = __ldcg(&rec[t * kRecSlots + slot0]);
+    }
+  };
+  int t = threadIdx.x;
+  for (; t + threads < count; t += 2 * threads) {
+    float2 x0[N], x1[N];
+    load(t, x0);
+    load(t + threads, x1);
+#pragma unroll
+    for (int q = 0; q < N; ++q) a[q] = df_add(df_add(a[q], df_of(x0[q])), df_of(x1[q]));
+  }
+  if (t < count) {
+    float2 x0[N];
+    load(t, x0);
+#pragma unroll
+    for (int q = 0; q < N; ++q) a[q] = df_add(a[q], df_of(x0[q]));
+  }
 }
 #endif
 
