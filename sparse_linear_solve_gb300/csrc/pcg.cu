@@ -155,6 +155,15 @@ __device__ __forceinline__ void timed_out(uint32_t* status, int* fail_sh) {
 }
 
 constexpr int kTileCache = 256;   // tiles per CTA whose block ranges stay in shared memory
+// Rows per thread of the update and direction phases loaded between the CTA's
+// barrier arrival and its wait (they are its own rows and need no scalar).
+// Each row moves about 3.7 MB of the phase's traffic into the wait on the
+// 1.65M-triangle cloth, about 0.5 us per iteration; five rows spill.
+#ifndef PCLOTH_PCG_PRE
+#define PCLOTH_PCG_PRE 4
+#endif
+constexpr int kPreRows = PCLOTH_PCG_PRE;
+static_assert(kPreRows >= 1, "at least one row loads under the barrier");
 
 struct LoopArgs {
   PipeMatrix m;
@@ -336,15 +345,23 @@ pcg_loop(LoopArgs a) {
       if (tid == 0) my_rec[REC_PQ] = df_pack(t[0]);
     }
     grid_arrive(a.bar, L.epoch, &fail_sh);
-    // The update's first row: its inputs are this CTA's own rows and do not
-    // depend on alpha, so they load while the other CTAs arrive.
-    const int32_t i_first = tid < nslots ? own_row(tid) : n;
-    float3 q_first = make_float3(0.f, 0.f, 0.f), r_first = q_first;
-    Sym3 p_first{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (i_first < n) {
-      q_first = ld3(a.q, a.vs, i_first);
-      r_first = ld3(a.r, a.vs, i_first);
-      p_first = ld_sym(a.pinv, a.vs, i_first);
+    // The update's first kPreRows rows of this thread: their inputs are this
+    // CTA's own rows and do not depend on alpha, so they load while the other
+    // CTAs arrive.  (Rows grow with the slot; past the end, i = n.)
+    int32_t i_pre[kPreRows];
+    float3 q_pre[kPreRows], r_pre[kPreRows];
+    Sym3 s_pre[kPreRows];
+#pragma unroll
+    for (int u = 0; u < kPreRows; ++u) {
+      const int32_t f = tid + u * kPipeThreads;
+      i_pre[u] = f < nslots ? min(own_row(f), n) : n;
+      q_pre[u] = r_pre[u] = make_float3(0.f, 0.f, 0.f);
+      s_pre[u] = Sym3{0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (i_pre[u] < n) {
+        q_pre[u] = ld3(a.q, a.vs, i_pre[u]);
+        r_pre[u] = ld3(a.r, a.vs, i_pre[u]);
+        s_pre[u] = ld_sym(a.pinv, a.vs, i_pre[u]);
+      }
     }
     if (!grid_wait(a.bar, L.epoch, &ok_sh)) break;
     if (timer) {
@@ -388,18 +405,21 @@ pcg_loop(LoopArgs a) {
         float* __restrict__ rv_ = a.r;
         float* __restrict__ zv_ = a.z;
         const int64_t vs = a.vs;
-        if (i_first < n) {
-          const float3 rn = make_float3(fmaf(-alpha, q_first.x, r_first.x),
-                                        fmaf(-alpha, q_first.y, r_first.y),
-                                        fmaf(-alpha, q_first.z, r_first.z));
-          const float3 zn = apply_p(p_first, rn);
-          st3(rv_, vs, i_first, rn);
-          st3(zv_, vs, i_first, zn);
-          arz += dot3(rn, zn);
-          arr += dot3(rn, rn);
+#pragma unroll
+        for (int u = 0; u < kPreRows; ++u) {
+          if (i_pre[u] < n) {
+            const float3 rn = make_float3(fmaf(-alpha, q_pre[u].x, r_pre[u].x),
+                                          fmaf(-alpha, q_pre[u].y, r_pre[u].y),
+                                          fmaf(-alpha, q_pre[u].z, r_pre[u].z));
+            const float3 zn = apply_p(s_pre[u], rn);
+            st3(rv_, vs, i_pre[u], rn);
+            st3(zv_, vs, i_pre[u], zn);
+            arz += dot3(rn, zn);
+            arr += dot3(rn, rn);
+          }
         }
 #pragma unroll 2
-        for (int32_t f = tid + kPipeThreads; f < nslots; f += kPipeThreads) {
+        for (int32_t f = tid + kPreRows * kPipeThreads; f < nslots; f += kPipeThreads) {
           const int32_t i = own_row(f);
           if (i >= n) break;   // rows grow with f: the rest are past the end too
           const float3 qv = ld3(qv_, vs, i), rv = ld3(rv_, vs, i);
@@ -421,14 +441,19 @@ pcg_loop(LoopArgs a) {
       }
     }
     grid_arrive(a.bar, L.epoch, &fail_sh);
-    // the direction phase's first row (the update's first row: this thread
-    // wrote its z), loaded while the other CTAs arrive
-    float4 pv_first = make_float4(0.f, 0.f, 0.f, 0.f);
-    float3 dv_first = make_float3(0.f, 0.f, 0.f), z_first = dv_first;
-    if (i_first < n) {
-      pv_first = a.p[i_first];
-      dv_first = ld3(a.dv, a.vs, i_first);
-      z_first = ld3(a.z, a.vs, i_first);
+    // the direction phase's first kPreRows rows (the update's: this thread
+    // wrote their z), loaded while the other CTAs arrive
+    float4 p_pre[kPreRows];
+    float3 d_pre[kPreRows], z_pre[kPreRows];
+#pragma unroll
+    for (int u = 0; u < kPreRows; ++u) {
+      p_pre[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      d_pre[u] = z_pre[u] = make_float3(0.f, 0.f, 0.f);
+      if (i_pre[u] < n) {
+        p_pre[u] = a.p[i_pre[u]];
+        d_pre[u] = ld3(a.dv, a.vs, i_pre[u]);
+        z_pre[u] = ld3(a.z, a.vs, i_pre[u]);
+      }
     }
     if (!grid_wait(a.bar, L.epoch, &ok_sh)) break;
     if (timer) {
@@ -479,17 +504,21 @@ pcg_loop(LoopArgs a) {
       float* __restrict__ dv_ = a.dv;
       const float* __restrict__ zv_ = a.z;
       const int64_t vs = a.vs;
-      if (i_first < n) {
-        const float4 pv = pv_first;
-        st3(dv_, vs, i_first,
-            make_float3(fmaf(alpha, pv.x, dv_first.x), fmaf(alpha, pv.y, dv_first.y),
-                        fmaf(alpha, pv.z, dv_first.z)));
-        if (!stop)
-          pv_[i_first] = make_float4(fmaf(beta, pv.x, z_first.x), fmaf(beta, pv.y, z_first.y),
-                                     fmaf(beta, pv.z, z_first.z), 0.f);
+#pragma unroll
+      for (int u = 0; u < kPreRows; ++u) {
+        if (i_pre[u] < n) {
+          const float4 pv = p_pre[u];
+          st3(dv_, vs, i_pre[u],
+              make_float3(fmaf(alpha, pv.x, d_pre[u].x), fmaf(alpha, pv.y, d_pre[u].y),
+                          fmaf(alpha, pv.z, d_pre[u].z)));
+          if (!stop)
+            pv_[i_pre[u]] = make_float4(fmaf(beta, pv.x, z_pre[u].x),
+                                        fmaf(beta, pv.y, z_pre[u].y),
+                                        fmaf(beta, pv.z, z_pre[u].z), 0.f);
+        }
       }
 #pragma unroll 2
-      for (int32_t f = tid + kPipeThreads; f < nslots; f += kPipeThreads) {
+      for (int32_t f = tid + kPreRows * kPipeThreads; f < nslots; f += kPipeThreads) {
         const int32_t i = own_row(f);
         if (i >= n) break;
         const float4 pv = pv_[i];
