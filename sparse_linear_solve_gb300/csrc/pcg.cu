@@ -21,10 +21,10 @@
 // Every scalar is formed by every CTA from the same per-CTA partials in the
 // same order (double-float sums), so all CTAs take the same decisions and
 // the solve is bitwise reproducible.  No host round trip happens inside the
-// solve.  The U phase loads its first row's inputs, which do not depend on
-// alpha, before it reduces p.q.  The vector phases are bound by memory
-// bandwidth, so the next SpMV's copies are not issued early: they would
-// compete with them.
+// solve.  A barrier's arrival and wait are separate, and a CTA uses the time
+// between them for work that needs nothing from the other CTAs: before U and
+// P each thread loads its first rows of the phase, before S thread 0 issues
+// the next SpMV's first stages.
 //
 // Every wait (mbarrier, grid barrier) is bounded in time: on a timeout the
 // CTA records ST_WAIT_TIMEOUT and marks its next barrier arrival, so that
@@ -164,6 +164,14 @@ constexpr int kTileCache = 256;   // tiles per CTA whose block ranges stay in sh
 #endif
 constexpr int kPreRows = PCLOTH_PCG_PRE;
 static_assert(kPreRows >= 1, "at least one row loads under the barrier");
+// Stages of the next SpMV that thread 0 issues between its CTA's arrival at
+// the direction phase's barrier and its wait: the matrix does not change, so
+// the copies need nothing from the other CTAs.  Two beat one and three on
+// the 1.65M-triangle cloth (67.9 against 69.5 and 68.6 us per iteration).
+#ifndef PCLOTH_PCG_EARLY
+#define PCLOTH_PCG_EARLY 2
+#endif
+constexpr int kEarlyStages = PCLOTH_PCG_EARLY;
 
 struct LoopArgs {
   PipeMatrix m;
@@ -532,7 +540,14 @@ pcg_loop(LoopArgs a) {
       }
     }
     if (stop) break;
-    if (!grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh)) break;
+    grid_arrive(a.bar, L.epoch, &fail_sh);
+    if (tid == 0) {
+      Producer P = L.P;
+      for (int j = 0; j < kEarlyStages && !P.ended; ++j)
+        if (producer_step<BW>(P, sh, m) < 0) timed_out(a.status, &fail_sh);
+      L.P = P;
+    }
+    if (!grid_wait(a.bar, L.epoch, &ok_sh)) break;
     if (timer) {
       const unsigned long long t = now_ns();
       L.t_p += t - L.t_prev;
