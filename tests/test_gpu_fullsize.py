@@ -5,9 +5,10 @@ Assembly (pattern bit-exact, every block) and SpMV are compared in full at
 every size; the oracle assembles a 10.9M-block system in seconds.  The fp64
 PCG of the two largest systems would take minutes on one host core, so there
 the solve is checked through properties that hold at any size: the recursive
-residual meets the tolerance, and the true residual |b - A dv| / |b| of the
+residual meets the tolerance, the true residual |b - A dv| / |b| of the
 GPU's dv, recomputed in fp64 with the oracle's own A and b, stays within the
-accuracy that fp32 storage allows.  The two smaller full configurations also
+accuracy that fp32 storage allows, and the iteration count matches the one
+the oracle's own solve of the same system recorded (oracle/iteration_table.py).  The two smaller full configurations also
 compare dv with the oracle's PCG directly.
 """
 import numpy as np
@@ -26,6 +27,16 @@ pytestmark = pytest.mark.gpu
 # recursion's fp32 rounding leaves the true residual above the recursive one
 # (up to ~1e-4 has been seen on the 32x32 grid); 1e-3 bounds it with margin.
 TRUE_RESIDUAL_BOUND = 1e-3
+
+
+def oracle_iterations(name):
+    """PCG iterations of the fp64 oracle on the first step of a configuration,
+    as oracle/iteration_table.py recorded them (same seeded inputs)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(oracle.__file__), "iteration_table.json")
+    with open(path) as f:
+        return int(json.load(f)[name]["iterations"][0])
 
 
 @pytest.mark.parametrize("name", ["C2", "C3"])
@@ -65,3 +76,7 @@ def test_fullsize_assembly_spmv_and_residual(name):
     d = dv.cpu().numpy().astype(np.float64)
     true = np.linalg.norm(ref.b - ref.spmv(d)) / np.linalg.norm(ref.b)
     assert true <= TRUE_RESIDUAL_BOUND, true
+    # the same PCG on the same system as the fp64 oracle's solve of this first
+    # step, whose iteration count oracle/iteration_table.py recorded
+    it_ref = oracle_iterations(name)
+    assert abs(it - it_ref) <= max(3, 0.03 * it_ref), (it, it_ref)
