@@ -97,6 +97,16 @@ def stored_traffic(kernel_src_digest):
     return None
 
 
+def traffic_per_launch(config, contacts, iterations_per_launch):
+    """ncu DRAM bytes of one PCG launch, from the committed capture scaled by
+    the launch's iterations: only while the kernel sources are the ones the
+    capture was taken on, and only for the workload it was taken on."""
+    per_it = stored_traffic(kernel_source_digest())
+    if per_it is None or (config, contacts) != TRAFFIC_WORKLOAD:
+        return None
+    return per_it * iterations_per_launch
+
+
 def kernel_source_digest():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -374,10 +384,7 @@ def run_ours(args, rank, world, local_rank):
                    d2h_bytes_per_step=int(2 * 12 * n),
                    pcg_iterations_mean=sum(e2e_its) / K)
 
-    traffic = None
-    per_it = stored_traffic(kernel_source_digest())
-    if per_it is not None and (args.config, args.contacts) == TRAFFIC_WORKLOAD:
-        traffic = per_it * iters / solves
+    traffic = traffic_per_launch(args.config, args.contacts, iters / solves)
     a_mb = nnzb * 28 / 1e6
     l2_note = ("inputs larger than L2: A is %.0f MB per step vs 129 MB L2" % a_mb if a_mb > 129 else
                "A (%.1f MB) fits in the 129 MB L2: L2-resident, not an HBM-bound case" % a_mb)
