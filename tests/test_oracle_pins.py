@@ -102,6 +102,26 @@ def test_two_vertex_closed_form_and_solve():
                                    atol=1e-12)
 
 
+def test_two_vertex_moving_rhs_at_advanced_positions():
+    """b = h f(x_t + h v_t) with both velocities nonzero (Eq. (3)), and A
+    unchanged by v (K at x_t).  Forces taken at x_t, at x_t + 2 h v_t, or
+    with either vertex's velocity dropped all give other values."""
+    g = load("two_vertex_moving.json")
+    x = np.array(g["x"], np.float32)
+    v = np.array(g["v"], np.float32)
+    s = oracle.assemble(2, np.array(g["mass"], np.float32), np.array(g["gravity"], np.float32),
+                        (np.array([0], np.int32), np.array([1], np.int32),
+                         np.array([g["k"]], np.float32), np.array([g["rest"]], np.float32)),
+                        None, x, v, g["h"])
+    assert s.status == oracle.OK
+    np.testing.assert_allclose(s.b.reshape(-1), np.array(g["b"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(s.dense(), np.array(g["A"]), rtol=0, atol=1e-12)
+    dv, it, rr, st = s.pcg(1e-14, 100)
+    assert st == oracle.OK
+    ref = np.linalg.solve(np.array(g["A"]), np.array(g["b"]))
+    np.testing.assert_allclose(dv.reshape(-1), ref, rtol=1e-10, atol=1e-12)
+
+
 def _tiny(n, rest_from_grid=False):
     return W.tiny_cloth(n=n, seed=1000 + n, rest_from_grid=rest_from_grid)
 
