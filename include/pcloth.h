@@ -225,20 +225,42 @@ int pcloth_profile_read(pcloth_t h, double* ms_out, int64_t* counts_out,
  * host application that reserves the GPU's memory for itself and forbids
  * plug-ins to allocate, or a real-time loop in which an allocation's latency
  * or failure mid-frame is unacceptable.  It solves A dv = b for a BSR3
- * matrix the caller already holds (rowptr int32[n+1], colind int32[nnzb]
- * sorted per row with the diagonal present, vals float32[nnzb][3][3], b
- * float32[n][3], all device pointers; dv float32[n][3] device output) with
- * the same block-Jacobi PCG as pcloth_solve, on the current device and the
- * given stream (a cudaStream_t, 0 = legacy default), and returns
- * *iterations and *rel_residual on the host.  It allocates nothing: all of
- * its scratch is one fixed array compiled into this library, which every
- * GPU that loads the library holds (about 1.5 MiB) until the process exits.
- * n may be at most PCLOTH_STATIC_MAX_VERTS; larger n returns
- * PCLOTH_ERR_CAPACITY without touching the GPU.  Every call on a device
- * shares that array, so calls that overlap on the GPU race: order them (one
- * stream, or events).  The first call on each device also looks up the
- * array's device address; make that first call before any stream capture.
- * Synchronises.  Errors are described by pcloth_last_error(NULL). */
+ * matrix the caller already holds, with the same block-Jacobi PCG as
+ * pcloth_solve, on the current device and the given stream (a cudaStream_t,
+ * 0 = legacy default), and returns *iterations and *rel_residual on the
+ * host.
+ *
+ * Arguments (device pointers, owned by the caller):
+ *   rowptr  int32[n+1], rowptr[0] = 0, non-decreasing;
+ *   colind  int32[rowptr[n]], each row's columns in [0, n), strictly
+ *           increasing, with the diagonal block present;
+ *   vals    float32[rowptr[n]][3][3], row-major blocks;
+ *   b       float32[n][3];  dv  float32[n][3] (output).
+ * A must be symmetric positive definite (so every diagonal block is
+ * symmetric); the preconditioner inverts each diagonal block from the six
+ * entries of its upper triangle.  rowptr, colind and vals must be 16-byte
+ * aligned (PCLOTH_ERR_INVALID_ARG otherwise, checked before any launch), and
+ * each must be followed by at least 16 bytes of readable device memory
+ * (for example the rest of a larger allocation): the solve streams them in
+ * whole 16-byte words, so its last copy of each can read up to 12 bytes past
+ * the end.  The pattern is checked on the device before the solve starts --
+ * reading rowptr and colind only as values -- and a malformed one returns
+ * PCLOTH_ERR_BAD_INDEX without launching the solve.
+ *
+ * It allocates nothing: all of its scratch is one fixed array compiled into
+ * this library, 1,513,216 bytes (about 1.44 MiB), which every GPU that loads
+ * the library holds until the process exits.  n may be at most
+ * PCLOTH_STATIC_MAX_VERTS; larger n returns PCLOTH_ERR_CAPACITY without
+ * touching the GPU.  Every call on a device shares that array, which keeps
+ * the last call's contents (each call sets up what it reads), so calls that
+ * overlap on the GPU race: order them (one stream, or events).
+ *
+ * The first call on each device looks up the array's device address and,
+ * with CUDA's lazy module loading, may be what loads this library's device
+ * code and with it the array itself: make one warm-up call at
+ * initialisation, before any window in which nothing may allocate and
+ * before any stream capture.  Synchronises (once after the pattern check,
+ * once at the end).  Errors are described by pcloth_last_error(NULL). */
 #define PCLOTH_STATIC_MAX_VERTS 16384
 int pcloth_solve_bsr3_static(int32_t n, const int32_t* rowptr, const int32_t* colind,
                              const float* vals, const float* b, double tol, int32_t maxit,

@@ -50,12 +50,14 @@ __global__ void bell_convert(int32_t n, int32_t W, const int32_t* __restrict__ r
 
 __global__ void __launch_bounds__(256)
 bell_spmv(int32_t n, int32_t W, const int32_t* __restrict__ col_ell,
-          const float* __restrict__ val_ell, const float* __restrict__ in,
-          float* __restrict__ out) {
+          const float* __restrict__ val_ell, const int32_t* __restrict__ rowptr,
+          const float* __restrict__ in, float* __restrict__ out) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const int64_t plane = int64_t(W) * n;
-  float ax = 0.f, ay = 0.f, az = 0.f;
+  // long rows are summed with compensation, as in the BSR3 kernel
+  const bool comp = rowptr[i + 1] - rowptr[i] > kCompRow;
+  float ax = 0.f, ay = 0.f, az = 0.f, cx = 0.f, cy = 0.f, cz = 0.f;
   for (int32_t s = 0; s < W; ++s) {
     const int64_t e = int64_t(s) * n + i;
     const int32_t c = col_ell[e];
@@ -66,13 +68,22 @@ bell_spmv(int32_t n, int32_t W, const int32_t* __restrict__ col_ell,
     const int64_t c3 = int64_t(c) * 3;
     const float x = in[c3], y = in[c3 + 1], z = in[c3 + 2];
     // the same products, in the same order, as the packed block of the BSR3 kernel
-    ax += fmaf(a00, x, fmaf(a01, y, a02 * z));
-    ay += fmaf(a01, x, fmaf(a11, y, a12 * z));
-    az += fmaf(a02, x, fmaf(a12, y, a22 * z));
+    const float px = fmaf(a00, x, fmaf(a01, y, a02 * z));
+    const float py = fmaf(a01, x, fmaf(a11, y, a12 * z));
+    const float pz = fmaf(a02, x, fmaf(a12, y, a22 * z));
+    if (comp) {
+      add_comp(ax, cx, px);
+      add_comp(ay, cy, py);
+      add_comp(az, cz, pz);
+    } else {
+      ax += px;
+      ay += py;
+      az += pz;
+    }
   }
-  out[3 * i] = ax;
-  out[3 * i + 1] = ay;
-  out[3 * i + 2] = az;
+  out[3 * i] = ax + cx;
+  out[3 * i + 1] = ay + cy;
+  out[3 * i + 2] = az + cz;
 }
 
 }  // namespace
@@ -117,7 +128,7 @@ int bell_build(Handle* h) {
 
 int launch_bell_spmv(Handle* h, const float* in, float* out) {
   bell_spmv<<<(h->n + 255) / 256, 256, 0, h->stream>>>(h->n, h->bell_w, h->bell_col, h->bell_val,
-                                                       in, out);
+                                                       h->rowptr, in, out);
   h->launches += 1;
   return check_launch(h, "bell spmv");
 }

@@ -782,17 +782,24 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
 
 // ===========================================================================
 // Allocation-free solve (pcloth_solve_bsr3_static).  It runs the same
-// persistent PCG on a general BSR3 system the caller already holds, and keeps
-// every work vector, every partial sum, the barrier counter and the status
-// words in one fixed array compiled into this library, so it never calls
-// cudaMalloc, cudaFree or any allocating routine.
+// persistent PCG on a symmetric positive-definite BSR3 system the caller
+// already holds, and keeps every work vector, every partial sum, the barrier
+// counter and the status words in one fixed array compiled into this
+// library, so it never calls cudaMalloc, cudaFree or any allocating routine.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
-// library holds it (about 1.5 MiB) until the process exits, and every call
-// on that GPU shares it.  Calls that overlap on the GPU therefore race on it;
-// a caller must order them (one stream, or events).  Each call re-initialises
-// everything it reads before reading it, so nothing leaks from one call into
-// the next.
+// library holds it (kStaticBytes = 1,513,216 bytes, about 1.44 MiB) until
+// the process exits, and every call on that GPU shares it.  Calls that
+// overlap on the GPU therefore race on it; a caller must order them (one
+// stream, or events).  Each call re-initialises everything it reads before
+// reading it, so nothing leaks from one call into the next.
+//
+// The caller's arrays are checked before the solve is launched: alignment on
+// the host, and the pattern on the device by a kernel that reads rowptr and
+// colind only as values (it reads colind[k] only for k inside a row range
+// it has already checked), so a malformed pattern is reported as
+// PCLOTH_ERR_BAD_INDEX instead of steering the solve's copies and gathers
+// out of bounds.
 // ===========================================================================
 namespace {
 
@@ -807,20 +814,50 @@ constexpr size_t kStaticBytes = sizeof(float4) * size_t(kStaticVec) +
                                 sizeof(float) * size_t(kStaticPlanes) * size_t(kStaticPlane) +
                                 sizeof(float2) * size_t(kRecSlots) * size_t(kStaticMaxRecords) +
                                 256;
+static_assert(kStaticBytes == 1513216, "the size the header states");
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
 // Device address of g_static_scratch per device ordinal (set up on first use).
 void* g_static_addr[64] = {};
 
+// Pattern check of a caller's BSR3 matrix, one thread per row: rowptr[0] = 0,
+// 0 <= rowptr[i] <= rowptr[i+1] <= rowptr[n], and inside the row every
+// column in [0, n), strictly increasing, with the diagonal present.  A row
+// whose bounds fail is not read further.  Any violation sets ST_BAD_INDEX.
+__global__ void bsr3_validate(int32_t n, const int32_t* __restrict__ rowptr,
+                              const int32_t* __restrict__ colind, uint32_t* status) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int32_t lo = rowptr[i], hi = rowptr[i + 1], total = rowptr[n];
+  bool ok = lo >= 0 && lo <= hi && hi <= total && (i != 0 || lo == 0);
+  if (ok) {
+    int32_t prev = -1;
+    bool diag = false;
+    for (int32_t k = lo; k < hi && ok; ++k) {
+      const int32_t c = colind[k];
+      ok = c > prev && c < n;
+      diag = diag || c == int32_t(i);
+      prev = c;
+    }
+    ok = ok && diag;
+  }
+  if (!ok) atomicOr(status, ST_BAD_INDEX);
+}
+
 // Inverse of the diagonal block of each row of a caller's BSR3 matrix, stored
-// like the library's own: six planes P00 P01 P02 P11 P12 P22 of vs floats.  A row without a
-// diagonal block, or with a non-invertible one, is reported as non-finite.
+// like the library's own: six planes P00 P01 P02 P11 P12 P22 of vs floats.
+// The block must be symmetric (A is symmetric positive definite): the
+// inverse is formed from the six cofactors of the upper triangle.  The block
+// is first scaled by its largest entry, so that the determinant of a tiny
+// (or huge) but well-conditioned block neither underflows nor overflows in
+// fp32; a block that is not positive definite by its determinant is
+// reported as non-finite.  The pattern has passed bsr3_validate, so the
+// diagonal is present.
 __global__ void bsr3_diag_inverse(int32_t n, const int32_t* __restrict__ rowptr,
                                   const int32_t* __restrict__ colind,
                                   const float* __restrict__ vals, float* __restrict__ pinv6,
-                                  int64_t vs,
-                                  uint32_t* status) {
+                                  int64_t vs, uint32_t* status) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   int32_t lo = rowptr[i], hi = rowptr[i + 1];
@@ -828,22 +865,26 @@ __global__ void bsr3_diag_inverse(int32_t n, const int32_t* __restrict__ rowptr,
     const int32_t mid = (lo + hi) >> 1;
     if (colind[mid] < i) lo = mid + 1; else hi = mid;
   }
-  float det = 0.f, c00 = 0.f, c01 = 0.f, c02 = 0.f, c11 = 0.f, c12 = 0.f, c22 = 0.f;
-  if (lo < rowptr[i + 1] && colind[lo] == i) {
-    const float* D = vals + 9 * int64_t(lo);
-    c00 = D[4] * D[8] - D[5] * D[7];
-    c01 = D[5] * D[6] - D[3] * D[8];
-    c02 = D[3] * D[7] - D[4] * D[6];
-    c11 = D[0] * D[8] - D[2] * D[6];
-    c12 = D[2] * D[3] - D[0] * D[5];
-    c22 = D[0] * D[4] - D[1] * D[3];
-    det = D[0] * c00 + D[1] * c01 + D[2] * c02;
-  }
-  if (!(det > 0.f) || !isfinite(det)) {
+  const float* D = vals + 9 * int64_t(lo);
+  float s = 0.f;
+#pragma unroll
+  for (int t = 0; t < 9; ++t) s = fmaxf(s, fabsf(D[t]));
+  const float inv_s = s > 0.f ? 1.0f / s : 0.f;
+  const float d00 = D[0] * inv_s, d01 = D[1] * inv_s, d02 = D[2] * inv_s;
+  const float d11 = D[4] * inv_s, d12 = D[5] * inv_s, d22 = D[8] * inv_s;
+  const float c00 = d11 * d22 - d12 * d12;
+  const float c01 = d12 * d02 - d01 * d22;
+  const float c02 = d01 * d12 - d11 * d02;
+  const float c11 = d00 * d22 - d02 * d02;
+  const float c12 = d02 * d01 - d00 * d12;
+  const float c22 = d00 * d11 - d01 * d01;
+  float det = d00 * c00 + d01 * c01 + d02 * c02;
+  if (!(det > 0.f) || !isfinite(det) || !(s > 0.f) || !isfinite(s)) {
     atomicOr(status, ST_NONFINITE);
     det = 1.f;
   }
-  const float id = 1.0f / det;
+  // (D / s)^-1 = s D^-1, so D^-1 = adj(D / s) / (det(D / s) s)
+  const float id = inv_s / det;
   pinv6[i] = c00 * id;
   pinv6[vs + i] = c01 * id;
   pinv6[2 * vs + i] = c02 * id;
@@ -857,6 +898,12 @@ __global__ void bsr3_diag_inverse(int32_t n, const int32_t* __restrict__ rowptr,
 int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, const float* vals,
                      const float* b, double tol, int32_t maxit, float* dv_out,
                      int32_t* iterations, double* rel_residual, cudaStream_t stream) {
+  // The solve streams rowptr, colind and vals with 16-byte bulk copies.
+  for (const void* p : {static_cast<const void*>(rowptr), static_cast<const void*>(colind),
+                        static_cast<const void*>(vals)})
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+      return fail(nullptr, PCLOTH_ERR_INVALID_ARG,
+                  "rowptr, colind and vals must be 16-byte aligned device pointers");
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
@@ -905,13 +952,24 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
 
   e = cudaMemsetAsync(tail, 0, 256, stream);   // state, status and barrier counter
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve reset");
+  // the pattern first: nothing below runs on a malformed one
+  bsr3_validate<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, status);
+  e = cudaGetLastError();
+  uint32_t st_bits = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&st_bits, status, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve pattern check");
+  if (st_bits & ST_BAD_INDEX)
+    return fail(nullptr, PCLOTH_ERR_BAD_INDEX,
+                "malformed BSR3 pattern: rowptr not starting at 0 or decreasing, a column "
+                "outside [0, n), columns of a row not strictly increasing, or no diagonal block");
   bsr3_diag_inverse<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, vals, pinv6,
                                                         kStaticPlane, status);
   e = cudaGetLastError();
   if (e == cudaSuccess) e = launch_loop<9>(a, grid, stream);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve launch");
   PcgState st{};
-  uint32_t st_bits = 0;
   e = cudaMemcpyAsync(&st, a.state, sizeof(PcgState), cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(&st_bits, status, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
@@ -921,7 +979,8 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
   if (rel_residual) *rel_residual = st.relres;
   if (st_bits & ST_WAIT_TIMEOUT) return fail(nullptr, PCLOTH_ERR_CUDA, "device wait timed out");
   if (st_bits & ST_NONFINITE)
-    return fail(nullptr, PCLOTH_ERR_NONFINITE, "non-finite value or missing/singular diagonal block");
+    return fail(nullptr, PCLOTH_ERR_NONFINITE,
+                "non-finite value, or a diagonal block that is not positive definite");
   if (st.code == PCLOTH_ERR_BREAKDOWN) return fail(nullptr, st.code, "PCG breakdown");
   if (st.code == PCLOTH_ERR_NONFINITE) return fail(nullptr, st.code, "non-finite value in PCG");
   return st.code;

@@ -49,6 +49,16 @@ constexpr int kAsmRows = 32;      // rows per assembly tile
 constexpr int kAsmCap = 768;      // blocks staged per assembly group
 constexpr int kAsmThreads = 256;
 
+// Rows of A longer than this many blocks are summed with compensation
+// (TwoSum) in every product A x: the plain fp32 sum of n products errs by up
+// to about n eps times the sum of their magnitudes, and a vertex in contact
+// with hundreds of others sums hundreds of terms that cancel to a small
+// fraction of their size.  Cloth rows (13 to 20 blocks) keep the plain sum,
+// which costs nothing; compensating every row cost 3% per PCG iteration and
+// 18% on the plain product.  The choice depends on the row's length only,
+// so the streaming and the block-ELL products agree bit for bit.
+constexpr int kCompRow = 32;
+
 constexpr int kVecThreads = 256;
 // Per-CTA partial sums of the PCG dot products, one double-float (float2)
 // per slot: p.q, r.z, r.r, b.b.
@@ -239,6 +249,17 @@ __device__ __forceinline__ Dfloat df_add(Dfloat a, Dfloat b) {
 }
 
 __device__ __forceinline__ Dfloat df_of(float x) { return Dfloat{x, 0.f}; }
+
+// Compensated running sum (TwoSum, Knuth): s + c carries the sum of the
+// terms added so far with the rounding error of every addition kept in c,
+// so a row of many terms that cancel (a vertex in contact with thousands of
+// others) loses nothing to the additions; read the total as s + c.
+__device__ __forceinline__ void add_comp(float& s, float& c, float x) {
+  const float t = s + x;
+  const float bp = t - s;
+  c += (s - (t - bp)) + (x - bp);
+  s = t;
+}
 __device__ __forceinline__ Dfloat df_of(float2 x) { return Dfloat{x.x, x.y}; }
 __device__ __forceinline__ float2 df_pack(Dfloat x) { return make_float2(x.hi, x.lo); }
 __device__ __forceinline__ double df_value(Dfloat x) { return double(x.hi) + double(x.lo); }

@@ -19,10 +19,10 @@
 //     block_times) by the gathered input vertex -- a thread issues all of
 //     its gathers before using any -- and stores the three products.  Two
 //     row warps take one thread per row of the tile: it adds its row's
-//     products in column order and hands the row to an epilogue.  The
-//     products are double-buffered and pass between the roles on mbarriers,
-//     so the row sums of one stage overlap the gathers of the next and are
-//     off the product warps' path.
+//     products in column order (rows longer than kCompRow blocks as a
+//     compensated TwoSum sum, see below) and hands the row to an epilogue.  The products are double-buffered and pass
+//     between the roles on mbarriers, so the row sums of one stage overlap
+//     the gathers of the next and are off the product warps' path.
 //
 // Tiles longer than a stage are split into chunks and the row sums carry
 // over, so every output has a fixed summation order and the product is
@@ -367,7 +367,7 @@ __device__ __forceinline__ bool consumer_pass(Consumer& C, const PipeShared& sh,
   const int ct = threadIdx.x - 32;
   const bool prod = ct < kPipeProd;
   const int rt = ct - kPipeProd;    // row thread index (row threads only)
-  float3 acc = make_float3(0.f, 0.f, 0.f);
+  float3 acc = make_float3(0.f, 0.f, 0.f), cmp = make_float3(0.f, 0.f, 0.f);
   while (true) {
     if (!wait_bounded(&sh.full[C.s], C.ph)) return false;
     const StageDesc d = sh.desc[C.s];
@@ -408,15 +408,24 @@ __device__ __forceinline__ bool consumer_pass(Consumer& C, const PipeShared& sh,
       const int32_t* rp = reinterpret_cast<const int32_t*>(st);
       const bool row_owner = rt < d.nrows;
       int32_t rs = 0, re = 0;
+      bool comp = false;
       if (row_owner) {
         rs = max(rp[rt], d.c0) - d.c0;
         re = min(rp[rt + 1], d.c1) - d.c0;
+        comp = rp[rt + 1] - rp[rt] > kCompRow;
         if (d.flags & 1) epi.begin(d.r0 + rt);
       }
       const int r0 = d.r0, last = d.flags & 2;
       mbar_arrive(&sh.empty[C.s]);   // desc and row pointers read
       if (!wait_bounded(&sh.ready[b], use)) return false;
-      if (row_owner) {
+      if (row_owner && comp) {
+        for (int32_t j = rs; j < re; ++j) {
+          const float4 t = part[j];
+          add_comp(acc.x, cmp.x, t.x);
+          add_comp(acc.y, cmp.y, t.y);
+          add_comp(acc.z, cmp.z, t.z);
+        }
+      } else if (row_owner) {
         for (int32_t j = rs; j < re; ++j) {
           const float4 t = part[j];
           acc.x += t.x;
@@ -426,8 +435,8 @@ __device__ __forceinline__ bool consumer_pass(Consumer& C, const PipeShared& sh,
       }
       mbar_arrive(&sh.freed[b]);
       if (row_owner && last) {
-        epi(r0 + rt, acc);
-        acc = make_float3(0.f, 0.f, 0.f);
+        epi(r0 + rt, make_float3(acc.x + cmp.x, acc.y + cmp.y, acc.z + cmp.z));
+        acc = cmp = make_float3(0.f, 0.f, 0.f);
       }
     }
     ++C.buf;

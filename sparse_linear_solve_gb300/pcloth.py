@@ -325,11 +325,14 @@ def pcloth_profile_read(h: int, reset: bool = False) -> dict:
 
 def pcloth_solve_bsr3_static(n: int, rowptr, colind, vals, b, tol: float, maxit: int, dv,
                              stream: Optional[int] = None):
-    """Allocation-free block-Jacobi PCG on a BSR3 system the caller holds
-    (device tensors: rowptr int32[n+1], colind int32[nnzb], vals float32
-    [nnzb,3,3], b float32[n,3]; dv float32[n,3] is written).  For callers
-    that must not allocate GPU memory; n <= STATIC_MAX_VERTS.  Returns
-    (iterations, rel_residual, code) like pcloth_solve."""
+    """Allocation-free block-Jacobi PCG on a symmetric positive-definite BSR3
+    system the caller holds (device tensors: rowptr int32[n+1], colind
+    int32[nnzb], vals float32[nnzb,3,3], b float32[n,3]; dv float32[n,3] is
+    written).  For callers that must not allocate GPU memory;
+    n <= STATIC_MAX_VERTS.  rowptr, colind and vals must start 16-byte
+    aligned and be followed by at least 16 readable bytes (e.g. views at the
+    start of larger tensors).  Returns (iterations, rel_residual, code) like
+    pcloth_solve."""
     ptrs = [None if t is None else t.data_ptr() for t in (rowptr, colind, vals, b, dv)]
     if stream is None:
         stream = torch.cuda.current_stream().cuda_stream

@@ -112,13 +112,9 @@ def test_contacts_duplicates_and_spring_pairs():
 
 def test_long_rows_exercise_chunked_paths():
     """One vertex in contact with 1500 others: its row is longer than the
-    assembly staging and the SpMV chunk, and a tile exceeds both.
-
-    The contacts are soft (k in [1, 10]) and near their rest lengths: with
-    contact stiffness 1e3 from one vertex to most of the cloth, the hub's
-    diagonal block reaches ~1e6 times its mass, and fp32 storage of that one
-    block alone moves the exact solution by ~2e-5; this test is about the
-    long-row code paths, not about that conditioning."""
+    assembly staging and the SpMV chunk, and a tile exceeds both.  Soft
+    contacts (k in [1, 10]) near their rest lengths; test_stiff_long_row is
+    the same row at contact stiffness."""
     w = W.tiny_cloth(n=48, rest_from_grid=True)
     N = w.n_verts
     hub = N // 2 + 7
@@ -137,6 +133,38 @@ def test_long_rows_exercise_chunked_paths():
     dv, it, rr, code = pcl.solve(w.tol, w.maxit)
     assert code == pc.OK
     assert rel_l2(dv.cpu().numpy(), dv_ref) <= 1e-4
+
+
+def test_stiff_long_row():
+    """The long-row case at contact stiffness: one vertex joined to 1500
+    others by contacts of k in [1e2, 1e3] and rest lengths in [1 mm, 5 cm].
+    The hub's diagonal block reaches ~8e5 times its mass, and the hub row of
+    every product A p sums 1500 terms that cancel to a small fraction of
+    their size.  Rounding A and b to fp32 (the storage) moves the exact
+    solution by 2.5e-5 (a direct fp64 solve of the rounded system against
+    the unrounded one); a plain fp32 sum of the hub row moves the PCG result
+    by ~4e-4, which the SpMV's compensated row sums remove.  Same 1e-4 bar
+    as every other PCG test."""
+    w = W.tiny_cloth(n=48, rest_from_grid=True)
+    N = w.n_verts
+    hub = N // 2 + 7
+    others = np.array([j for j in range(N) if j != hub][:1500], np.int32)
+    rng = np.random.default_rng(5)
+    c = W.Contacts(np.full(len(others), hub, np.int32), others,
+                   rng.uniform(1e2, 1e3, len(others)).astype(np.float32),
+                   rng.uniform(1e-3, 5e-2, len(others)).astype(np.float32))
+    w.max_contacts = len(others)
+    pcl, ref, g, _ = compare_assembly(w, w.x0, w.v0, c)
+    assert int(g["rowptr"][hub + 1] - g["rowptr"][hub]) > 1024
+    x = np.random.default_rng(2).normal(size=(N, 3)).astype(np.float32)
+    assert rel_l2(pcl.spmv(to_dev(x)).cpu().numpy(), ref.spmv(x)) <= 1e-5
+    dv_ref, it_ref, _, st = ref.pcg(w.tol, w.maxit)
+    assert st == oracle.OK
+    dv, it, rr, code = pcl.solve(w.tol, w.maxit)
+    assert code == pc.OK
+    e = rel_l2(dv.cpu().numpy(), dv_ref)
+    assert e <= 1e-4, (e, it, it_ref)
+    assert abs(it - it_ref) <= max(3, 0.03 * it_ref), (it, it_ref)
 
 
 def test_pattern_rebuilt_in_place_across_steps():
