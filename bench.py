@@ -63,6 +63,20 @@ def workload_desc(w):
                 h=w.h, tol=w.tol, maxit=w.maxit)
 
 
+def bench_config(w):
+    """The `config` of both arms' JSON lines (identical, so that the two
+    lines compare): the workload, the parallelism and the L2 statement.  The
+    matrix size is the bound from the workload's counts: 28 B per block (24 B
+    of packed symmetric values + the column), for the diagonal and both
+    directions of every spring and contact."""
+    a_mb = 28 * (w.n_verts + 2 * (w.n_springs + w.max_contacts)) / 1e6
+    l2 = ("inputs larger than L2: A is about %.0f MB per step vs 129 MB L2" % a_mb if a_mb > 129
+          else "A (about %.1f MB) fits in the 129 MB L2: L2-resident, not an HBM-bound case"
+          % a_mb)
+    return dict(workload_desc(w), parallelism="replicas only (one independent cloth per GPU)",
+                l2=l2)
+
+
 # ------------------------------------------------------------------ peaks --
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -181,17 +195,25 @@ def oracle_sample(w, x, v, contacts, iters):
     return t1 - t0, (t2 - t1) / max(iters, 1)
 
 
-def oracle_iterations_per_step(config, fallback):
-    """PCG iterations the oracle needs per step, from the committed table
-    written by oracle/iteration_table.py (fp64 oracle runs only)."""
+def oracle_step_iterations(config):
+    """PCG iterations the oracle needs at each step of its own trajectory,
+    from the committed table written by oracle/iteration_table.py (fp64
+    oracle runs only); an empty list if the table has none."""
     path = os.path.join(ROOT, "oracle", "iteration_table.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-        its = d[config]["iterations"]
-        return float(sum(its)) / len(its), "oracle table (%d steps)" % len(its)
+            return [int(i) for i in json.load(f)[config]["iterations"]]
     except Exception:
-        return float(fallback), "GPU mean iteration count (oracle table absent)"
+        return []
+
+
+def oracle_whole_step(w, x, v, contacts):
+    """Time one whole implicit step of the fp64 oracle (assembly, PCG to the
+    workload's tolerance, state update).  Returns (seconds, iterations)."""
+    from oracle import oracle
+    t0 = time.perf_counter()
+    res = oracle.step(w, x, v, contacts)
+    return time.perf_counter() - t0, int(res.get("iterations", 0))
 
 
 # ------------------------------------------------------------- ranks --
@@ -385,16 +407,12 @@ def run_ours(args, rank, world, local_rank):
                    pcg_iterations_mean=sum(e2e_its) / K)
 
     traffic = traffic_per_launch(args.config, args.contacts, iters / solves)
-    a_mb = nnzb * 28 / 1e6
-    l2_note = ("inputs larger than L2: A is %.0f MB per step vs 129 MB L2" % a_mb if a_mb > 129 else
-               "A (%.1f MB) fits in the 129 MB L2: L2-resident, not an HBM-bound case" % a_mb)
     result = dict(
         metric=METRIC, value=whole_job_rate(world, K, ms * 1e-3), unit=UNIT, n_gpus=world, steps=K,
         warmup=Wm, ms_per_step=ms / K, higher_is_better=True, scaling="weak",
         vs_baseline=None, dtype="f32 (fp32 storage and arithmetic; PCG dot products reduced as fp32 pairs, double-float)",
         data="synthetic (seeded generator; no garment meshes available)",
-        config=dict(workload_desc(w), parallelism="replicas only (one independent cloth per GPU)",
-                    l2=l2_note),
+        config=bench_config(w),
         pcg_iterations_per_s=whole_job_rate(world, sum(its), ms * 1e-3),
         pcg_iterations_per_s_solve_only=sum(its_prof) / (prof["solve_ms"] * 1e-3),
         pcg_iterations_mean=sum(its) / K,
@@ -431,43 +449,62 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_layouts:
         result["spmv_layouts"] = spmv_layouts(cloth, n, dev)
 
-    # ---- CPU baseline: the oracle on the host cores, bounded sample ------
+    # ---- CPU baseline: the oracle on the host cores, one whole step -------
+    # the first timed step, from the same state and contacts as the GPU's
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         c = host_contacts[Wm]
-        t_asm, t_it = oracle_sample(w, w.x0, w.v0, c if c.n else None, args.oracle_iters)
-        it_step, src = oracle_iterations_per_step(args.config, sum(its) / K)
-        step_s = t_asm + it_step * t_it
+        step_s, it_o = oracle_whole_step(w, x_start.cpu().numpy(), v_start.cpu().numpy(),
+                                         c if c.n else None)
         result["cpu_baseline"] = dict(
             value=1.0 / step_s, unit=UNIT, cores=1, kind="oracle",
-            sample="fp64 C++ oracle, one thread: full assembly of one step (%.2f s) plus %d PCG "
-                   "iterations (%.3f s each), extrapolated to %.0f iterations per step (%s)"
-                   % (t_asm, args.oracle_iters, t_it, it_step, src))
+            sample="fp64 C++ oracle, one thread: one whole implicit step (assembly, PCG to "
+                   "%g, update; %.1f s, measured, not extrapolated) -- the first timed step, "
+                   "from the GPU's state and contacts of that step; PCG iterations: oracle %d, "
+                   "GPU %d" % (w.tol, step_s, it_o, its[0]),
+            iterations=it_o, gpu_iterations=its[0])
     cloth.close()
     return result
 
 
 def run_reference(args):
-    """The fp64 oracle on the host cores, same config, metric and unit."""
+    """The fp64 oracle on the host cores, same config, metric and unit.
+
+    A whole oracle step takes tens of seconds, so each step is a bounded
+    sample -- the step's full assembly plus a few PCG iterations, timed --
+    extrapolated to a whole step with the oracle's own iteration count for
+    that step of its trajectory (oracle/iteration_table.json).  The line
+    says so: `extrapolated` is true and `ms_per_step` is not wall time."""
     from sparse_linear_solve_gb300 import workloads as W
     w = W.make(args.config)
     K, Wm = args.steps, args.warmup
-    it_step, src = oracle_iterations_per_step(args.config, 1000)
-    samples = []
+    table = oracle_step_iterations(args.config)
+    mean_it = float(sum(table)) / len(table) if table else float(w.maxit)
+    samples, its = [], []
+    wall0 = time.perf_counter()
     for t in range(Wm + K):
         c = w.contacts(t)
         iters = args.oracle_iters if t >= Wm else 1
         t_asm, t_it = oracle_sample(w, w.x0, w.v0, c if c.n else None, iters)
         if t >= Wm:
-            samples.append(t_asm + it_step * t_it)
+            it_t = table[t] if t < len(table) else mean_it
+            its.append(it_t)
+            samples.append(t_asm + it_t * t_it)
+    wall = time.perf_counter() - wall0
     step_s = sum(samples) / len(samples)
     value = 1.0 / step_s
-    sample = ("fp64 C++ oracle, one thread: per step the full assembly plus %d PCG iterations, "
-              "extrapolated to %.0f iterations per step (%s)" % (args.oracle_iters, it_step, src))
+    src = ("the oracle's own trajectory, steps %d-%d" % (Wm, Wm + K - 1)
+           if Wm + K <= len(table) else
+           "the oracle's trajectory table (%d steps; its mean past them)" % len(table))
+    sample = ("EXTRAPOLATED, not measured whole: fp64 C++ oracle, one thread; per step the "
+              "full assembly plus %d PCG iterations timed at the initial state, scaled to "
+              "the PCG iterations of that step (%s; mean %.1f); %.1f s of wall time in all"
+              % (args.oracle_iters, src, sum(its) / len(its), wall))
     return dict(metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=K, warmup=Wm,
                 ms_per_step=step_s * 1e3, higher_is_better=True, scaling="weak",
                 vs_baseline=None, dtype="f64", data="synthetic",
-                config=dict(workload_desc(w), parallelism="host, 1 thread"),
-                impl="reference",
+                config=bench_config(w),
+                impl="reference", extrapolated=True, wall_s=wall,
+                pcg_iterations_mean=sum(its) / len(its),
                 cpu_baseline=dict(kind="oracle", cores=1, sample=sample, value=value, unit=UNIT),
                 e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 

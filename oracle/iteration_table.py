@@ -1,16 +1,22 @@
-"""Record how many PCG iterations the fp64 oracle needs on the first step of
-each named configuration (test infrastructure).
+"""Record how many PCG iterations the fp64 oracle needs per step of each named
+configuration along its own trajectory (test infrastructure).
 
-The benchmark's CPU baseline times the oracle on a bounded sample (one
-assembly plus a few PCG iterations) and extrapolates to a whole step with the
-counts stored here.  Only the oracle and the seeded input generators run.
+Step t starts from the oracle's state after step t-1 (x and v updated with
+the oracle's own dv) with that step's contact list, as the benchmark's steps
+do on the GPU.  The benchmark's reference arm times the oracle on a bounded
+sample (one assembly plus a few PCG iterations) and scales it to each step
+with the counts stored here.  Only the oracle and the seeded input
+generators run.
 
-    python -m oracle.iteration_table C1 C2 C3 C4 C5
+    python -m oracle.iteration_table [--steps S] C1 C2 C3 C4 C5
 """
+import argparse
 import json
 import os
 import sys
 import time
+
+import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, os.path.dirname(HERE))
@@ -21,23 +27,34 @@ from sparse_linear_solve_gb300 import workloads as W  # noqa: E402
 TABLE = os.path.join(HERE, "iteration_table.json")
 
 
-def main(names):
+def main(names, steps):
     table = {}
     if os.path.exists(TABLE):
         with open(TABLE) as f:
             table = json.load(f)
     for name in names:
         w = W.make(name)
-        c = w.contacts(0)
-        t0 = time.perf_counter()
-        s = oracle.assemble_workload(w, w.x0, w.v0, c if c.n else None)
-        dv, it, rr, st = s.pcg(w.tol, w.maxit)
-        table[name] = dict(iterations=[it], relres=[rr], status=[st], steps=[0],
-                           tol=w.tol, seconds=time.perf_counter() - t0)
-        print(name, table[name], flush=True)
-        with open(TABLE, "w") as f:
-            json.dump(table, f, indent=1, sort_keys=True)
+        x, v = w.x0, w.v0
+        its, rrs, sts, secs = [], [], [], []
+        for t in range(steps):
+            c = w.contacts(t)
+            t0 = time.perf_counter()
+            res = oracle.step(w, x, v, c if c.n else None)
+            secs.append(time.perf_counter() - t0)
+            its.append(int(res["iterations"]))
+            rrs.append(float(res["relres"]))
+            sts.append(int(res["status"]))
+            x, v = res["x"].astype(np.float32), res["v"].astype(np.float32)
+            table[name] = dict(iterations=its, relres=rrs, status=sts, steps=list(range(len(its))),
+                               tol=w.tol, seconds=secs)
+            print(name, t, its[-1], "%.1f s" % secs[-1], flush=True)
+            with open(TABLE, "w") as f:
+                json.dump(table, f, indent=1, sort_keys=True)
 
 
 if __name__ == "__main__":
-    main(sys.argv[1:] or ["C1", "C2", "C3", "C4", "C5"])
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--steps", type=int, default=1)
+    ap.add_argument("names", nargs="*", default=["C1", "C2", "C3", "C4", "C5"])
+    a = ap.parse_args()
+    main(a.names, a.steps)

@@ -35,8 +35,8 @@ void free_handle(Handle* h) {
   void* bufs[] = {h->mass, h->rowptr_s, h->colind_s, h->sblk_ptr, h->sentry,
                   h->rowptr, h->colind, h->vals, h->rhs, h->pinv6,
                   h->ckey[0], h->ckey[1], h->cval[0], h->cval[1],
-                  h->sort_counts, h->flags, h->scan_tmp, h->newkey,
-                  h->newfirst, h->tile_nb, h->tile_eb, h->counters,
+                  h->sort_counts, h->scan_tmp, h->rowcnt, h->newcnt, h->newcol,
+                  h->newfirst, h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
                   h->dv, h->dv3, h->r3, h->z3, h->p4, h->q3, h->rec, h->bar,
                   h->phase_ns, h->state, h->d_status, h->bell_wmax, h->bell_col, h->bell_val,
@@ -203,8 +203,8 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   const int64_t ent2 = std::max<int64_t>(2 * mc, 1);
   // the radix sort also orders the n vertices by cell for contact finding
   const int64_t sort_tiles = (std::max<int64_t>(ent2, n) + kSortTile - 1) / kSortTile;
-  const int64_t scan_tiles = (ent2 + kScanTile - 1) / kScanTile;
-  const int64_t asm_tiles = (n + kAsmRows - 1) / kAsmRows;
+  // scans run over the n + 1 per-row counts of the assembly
+  const int64_t scan_tiles = (std::max<int64_t>(ent2, n + 1) + kScanTile - 1) / kScanTile;
   h->spmv_grid = spmv_grid_for(int32_t(n), h->sm_count);
   {
     const int ge = pcg_loop_grid(kSymBlock, int32_t(n), h->device, h->sm_count, &h->loop_grid);
@@ -237,12 +237,11 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
     A(dalloc(&h->vid[b], n));
   }
   A(dalloc(&h->sort_counts, sort_tiles * kSortRadix + 1));
-  A(dalloc(&h->flags, ent2 + 1));
   A(dalloc(&h->scan_tmp, scan_tiles + 1));
-  A(dalloc(&h->newkey, ent2));
+  A(dalloc(&h->rowcnt, 2 * (n + 1)));
+  A(dalloc(&h->newcnt, n + 1));
+  A(dalloc(&h->newcol, ent2));
   A(dalloc(&h->newfirst, ent2));
-  A(dalloc(&h->tile_nb, asm_tiles + 1));
-  A(dalloc(&h->tile_eb, asm_tiles + 1));
   A(dalloc(&h->counters, 4));
   A(dalloc(&h->hx, 3 * n));
   A(dalloc(&h->hv, 3 * n));

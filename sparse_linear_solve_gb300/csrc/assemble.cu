@@ -2,21 +2,26 @@
 // Eq. (3) for the system, Sec. 3.2 for the assembly elements, Sec. 3.2.2 for
 // the sparse matrix filling).
 //
-// The page fills an ELL index table with atomics, sorts and compacts each row
-// with one thread per row, then fills values with atomics.  This design keeps
-// BSR3 and replaces those steps with deterministic ones:
+// The page fills an index table with atomics, sorts and compacts each row
+// with one thread per row, then fills values with atomics.  Here the spring
+// pattern is built once (pcloth_create) and each step's contacts go through
+// the same steps, made deterministic:
 //
-//   contact_keys     two directed keys (row << B | col) per contact
-//   radix sort       stable, so equal keys keep their input order
-//   contact_classify flag the first entry of every (row, col) pair that is
-//                    not already a block of the static spring pattern
-//   scan + compact   list of new blocks, sorted by (row, col)
-//   tile_bounds      per tile of rows: first new block / first entry
-//   assemble_rows    per tile: rebuild rowptr and colind in place (static
-//                    blocks shifted by the new blocks of earlier rows, new
-//                    blocks merged into their rows), evaluate every element
-//                    of every off-diagonal block, reduce each row into its
-//                    diagonal block, b = h f and the block-Jacobi inverse.
+//   contact_count     entries per row (a contact (i, j) is an entry of row i
+//                     with column j and one of row j with column i), atomics
+//   scan              first entry of each row
+//   contact_scatter   the entries into their rows (any order within a row)
+//   row_classify      one thread per row sorts its entries by (column,
+//                     contact id) -- so equal blocks sum in input order --
+//                     and lists the columns that are not spring blocks: the
+//                     row's new blocks
+//   scan              new blocks before each row
+//   assemble_rows     16 lanes per row: the row's blocks in column order
+//                     (spring and new blocks merged), every element of every
+//                     off-diagonal block evaluated and written, the row's
+//                     compensated sum into its diagonal block, b = h f and
+//                     the block-Jacobi inverse.  No shared memory, no CTA
+//                     barrier: rows are independent.
 //
 // No float atomics: every sum has a fixed order, so the assembled system is
 // bitwise reproducible.  Each off-diagonal block is computed by its own row;
@@ -31,13 +36,14 @@
 namespace pcloth_impl {
 namespace {
 
-constexpr uint64_t kSentinel = ~0ull;
-constexpr int kRowLanes = kAsmThreads / kAsmRows;   // threads per row in the row reductions
-static_assert(kRowLanes == 8, "the row reduction merges eight lanes");
+#ifndef PCLOTH_ASM_LANES
+#define PCLOTH_ASM_LANES 2
+#endif
+constexpr int kRowLanes = PCLOTH_ASM_LANES;   // lanes of a warp that assemble one row
+static_assert(kAsmThreads % 32 == 0 && 32 % kRowLanes == 0, "whole rows per warp");
 
 struct AsmArgs {
   int32_t n;
-  int B;                 // bits per index in a key
   float dt, h2;
   float gx, gy, gz;
   const float* x;
@@ -48,38 +54,92 @@ struct AsmArgs {
   const int32_t* sblk_ptr;
   const float2* sentry;
   int has_contacts;
-  const uint64_t* skey;    // sorted contact keys
-  const int32_t* sval;     // contact id of each sorted key
+  const int32_t* ebefore;   // [n+1] first contact entry of each row
+  const int32_t* nbefore;   // [n+1] new blocks before each row
+  const uint64_t* centry;   // entries, per row sorted by (column << 32 | contact id)
+  const int32_t* newcol;    // a row's new columns, at the row's first entry index
+  const int32_t* newfirst;  // the entry index of each new column's first entry
   const float* ck;
   const float* cr;
-  const uint64_t* newkey;
-  const int32_t* newfirst;
-  const int32_t* tile_nb;
-  const int32_t* tile_eb;
-  const int32_t* counters;  // [0] new blocks, [1] valid entries
   int32_t* rowptr;
   int32_t* colind;
-  float* vals;
+  float* vals;        // packed symmetric blocks, six floats each
   float* rhs;
   float* pinv6;      // [6][vs]
   int64_t vs;
   uint32_t* status;
 };
 
-__global__ void contact_keys(int32_t nc, int32_t n, int B, const int32_t* __restrict__ ci,
-                             const int32_t* __restrict__ cj, const float* __restrict__ ck,
-                             const float* __restrict__ cr, uint64_t* __restrict__ keys,
-                             int32_t* __restrict__ vals, uint32_t* status) {
+// The one validity test of a contact, shared by the counting and the
+// scattering pass so that both skip the same contacts.
+__device__ __forceinline__ bool contact_ok(int32_t i, int32_t j, int32_t n) {
+  return i >= 0 && i < n && j >= 0 && j < n && i != j;
+}
+
+__global__ void contact_count(int32_t nc, int32_t n, const int32_t* __restrict__ ci,
+                              const int32_t* __restrict__ cj, const float* __restrict__ ck,
+                              const float* __restrict__ cr, int32_t* __restrict__ rowcnt,
+                              uint32_t* status) {
   const int32_t c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= nc) return;
   const int32_t i = ci[c], j = cj[c];
-  const bool ok = i >= 0 && i < n && j >= 0 && j < n && i != j;
-  if (!ok) atomicOr(status, ST_BAD_INDEX);
   if (!isfinite(ck[c]) || !isfinite(cr[c])) atomicOr(status, ST_NONFINITE);
-  keys[2 * int64_t(c)] = ok ? (uint64_t(i) << B) | uint64_t(j) : kSentinel;
-  keys[2 * int64_t(c) + 1] = ok ? (uint64_t(j) << B) | uint64_t(i) : kSentinel;
-  vals[2 * int64_t(c)] = c;
-  vals[2 * int64_t(c) + 1] = c;
+  if (!contact_ok(i, j, n)) {
+    atomicOr(status, ST_BAD_INDEX);
+    return;
+  }
+  atomicAdd(&rowcnt[i], 1);
+  atomicAdd(&rowcnt[j], 1);
+}
+
+__global__ void contact_scatter(int32_t nc, int32_t n, const int32_t* __restrict__ ci,
+                                const int32_t* __restrict__ cj,
+                                const int32_t* __restrict__ ebefore, int32_t* __restrict__ fill,
+                                uint64_t* __restrict__ centry) {
+  const int32_t c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= nc) return;
+  const int32_t i = ci[c], j = cj[c];
+  if (!contact_ok(i, j, n)) return;
+  const int32_t pi = ebefore[i] + atomicAdd(&fill[i], 1);
+  const int32_t pj = ebefore[j] + atomicAdd(&fill[j], 1);
+  centry[pi] = (uint64_t(uint32_t(j)) << 32) | uint32_t(c);
+  centry[pj] = (uint64_t(uint32_t(i)) << 32) | uint32_t(c);
+}
+
+// Sorts a row's few entries in place: insertion sort, or heapsort for long
+// rows (a vertex in contact with hundreds of others).
+__device__ __forceinline__ void sort_entries(uint64_t* a, int32_t m) {
+  if (m <= 32) {
+    for (int32_t t = 1; t < m; ++t) {
+      const uint64_t key = a[t];
+      int32_t u = t - 1;
+      while (u >= 0 && a[u] > key) {
+        a[u + 1] = a[u];
+        --u;
+      }
+      a[u + 1] = key;
+    }
+    return;
+  }
+  auto sift = [&](int32_t root, int32_t end) {   // max-heap on [0, end)
+    while (true) {
+      int32_t child = 2 * root + 1;
+      if (child >= end) return;
+      if (child + 1 < end && a[child + 1] > a[child]) ++child;
+      if (a[root] >= a[child]) return;
+      const uint64_t t = a[root];
+      a[root] = a[child];
+      a[child] = t;
+      root = child;
+    }
+  };
+  for (int32_t r = m / 2 - 1; r >= 0; --r) sift(r, m);
+  for (int32_t end = m - 1; end > 0; --end) {
+    const uint64_t t = a[0];
+    a[0] = a[end];
+    a[end] = t;
+    sift(0, end);
+  }
 }
 
 __device__ __forceinline__ bool static_has(const int32_t* __restrict__ colind_s,
@@ -93,63 +153,45 @@ __device__ __forceinline__ bool static_has(const int32_t* __restrict__ colind_s,
   return false;
 }
 
-__global__ void contact_classify(int32_t m, int B, const uint64_t* __restrict__ skey,
-                                 const int32_t* __restrict__ rowptr_s,
-                                 const int32_t* __restrict__ colind_s,
-                                 int32_t* __restrict__ flags, int32_t* __restrict__ counters) {
-  const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= m) return;
-  const uint64_t key = skey[t];
-  int32_t f = 0;
-  if (key != kSentinel) {
-    const uint64_t mask = (uint64_t(1) << B) - 1;
-    const int32_t row = int32_t(key >> B), col = int32_t(key & mask);
-    const bool first = (t == 0) || skey[t - 1] != key;
-    if (first && !static_has(colind_s, rowptr_s[row], rowptr_s[row + 1], col)) f = 1;
-    // sentinels sort last: the last valid entry records the valid count
-    if (t + 1 == m || skey[t + 1] == kSentinel) counters[1] = t + 1;
+// One thread per row (thread n writes newcnt[n] = 0, the scan's total slot).
+__global__ void row_classify(int32_t n, const int32_t* __restrict__ ebefore,
+                             uint64_t* __restrict__ centry, const int32_t* __restrict__ rowptr_s,
+                             const int32_t* __restrict__ colind_s, int32_t* __restrict__ newcol,
+                             int32_t* __restrict__ newfirst, int32_t* __restrict__ newcnt) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i > n) return;
+  if (i == n) {
+    newcnt[n] = 0;
+    return;
   }
-  flags[t] = f;
+  const int32_t e0 = ebefore[i], e1 = ebefore[i + 1];
+  int32_t k = 0;
+  if (e1 > e0) {
+    sort_entries(centry + e0, e1 - e0);
+    const int32_t s0 = rowptr_s[i], s1 = rowptr_s[i + 1];
+    int32_t last = -1;
+    for (int32_t t = e0; t < e1; ++t) {
+      const int32_t col = int32_t(centry[t] >> 32);
+      if (col == last) continue;
+      last = col;
+      if (!static_has(colind_s, s0, s1, col)) {
+        newcol[e0 + k] = col;
+        newfirst[e0 + k] = t;
+        ++k;
+      }
+    }
+  }
+  newcnt[i] = k;
 }
 
-__global__ void contact_compact(int32_t m, const uint64_t* __restrict__ skey,
-                                const int32_t* __restrict__ prefix,
-                                const int32_t* __restrict__ counters,
-                                uint64_t* __restrict__ newkey, int32_t* __restrict__ newfirst) {
-  const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= m) return;
-  const int32_t next = (t + 1 < m) ? prefix[t + 1] : counters[0];
-  if (next != prefix[t]) {
-    newkey[prefix[t]] = skey[t];
-    newfirst[prefix[t]] = t;
-  }
-}
-
-__device__ __forceinline__ int32_t lower_bound_key(const uint64_t* __restrict__ a,
-                                                   int32_t lo, int32_t hi, uint64_t key) {
+__device__ __forceinline__ int32_t lower_bound_col(const uint64_t* __restrict__ a, int32_t lo,
+                                                   int32_t hi, int32_t col) {
+  const uint64_t key = uint64_t(uint32_t(col)) << 32;
   while (lo < hi) {
     const int32_t mid = (lo + hi) >> 1;
     if (a[mid] < key) lo = mid + 1; else hi = mid;
   }
   return lo;
-}
-
-__global__ void tile_bounds(int32_t ntiles, int32_t n, int B, int has_contacts,
-                            const uint64_t* __restrict__ newkey,
-                            const uint64_t* __restrict__ skey,
-                            const int32_t* __restrict__ counters,
-                            int32_t* __restrict__ tile_nb, int32_t* __restrict__ tile_eb) {
-  const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t > ntiles) return;
-  if (!has_contacts) {
-    tile_nb[t] = 0;
-    tile_eb[t] = 0;
-    return;
-  }
-  const int64_t r = min(int64_t(t) * kAsmRows, int64_t(n));
-  const uint64_t key = uint64_t(r) << B;
-  tile_nb[t] = lower_bound_key(newkey, 0, counters[0], key);
-  tile_eb[t] = lower_bound_key(skey, 0, counters[1], key);
 }
 
 // An edge vector carried exactly as hi + lo: the difference of two fp32
@@ -264,94 +306,32 @@ __device__ __forceinline__ float3 ld3(const float* p, int64_t i) {
 }
 
 // Merge position p of two sorted disjoint lists S (static cols) and T (new
-// contact cols): returns a = number of S entries before position p.
+
+// Merge position p of two sorted disjoint column lists S (spring blocks) and
+// T (new blocks): returns the number of S entries before position p.
 __device__ __forceinline__ int32_t merge_split(const int32_t* __restrict__ S, int32_t nS,
-                                               const uint64_t* __restrict__ T, int32_t nT,
-                                               uint64_t mask, int32_t p) {
+                                               const int32_t* __restrict__ T, int32_t nT,
+                                               int32_t p) {
   int32_t lo = max(0, p - nT), hi = min(p, nS);
   while (lo < hi) {
     const int32_t mid = (lo + hi + 1) >> 1;
-    if (S[mid - 1] < int32_t(T[p - mid] & mask)) lo = mid; else hi = mid - 1;
+    if (S[mid - 1] < T[p - mid]) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
-struct RowInfo {
-  int32_t sb, se;   // static slots
-  int32_t nb, ne;   // new blocks
-  int32_t eb, ee;   // sorted contact entries
-  int32_t ob;       // first output block
-};
-
-// Computes block `o` (absolute output index) of tile-local row `ri`; writes
-// the value (-h^2 sum K as a packed symmetric block, 6 floats) and the force
-// sum into shared staging.
-__device__ __forceinline__ void compute_block(const AsmArgs& a, int32_t i, const RowInfo& R,
-                                              int32_t p, float* __restrict__ stv,
-                                              float* __restrict__ stf, int32_t* __restrict__ stc,
-                                              int32_t m_valid) {
-  const uint64_t mask = (uint64_t(1) << a.B) - 1;
-  const int32_t nS = R.se - R.sb, nT = R.ne - R.nb;
-  int32_t col, sslot = -1, nk = -1;
-  if (nT == 0) {
-    sslot = R.sb + p;
-    col = a.colind_s[sslot];
-  } else {
-    const int32_t s = merge_split(a.colind_s + R.sb, nS, a.newkey + R.nb, nT, mask, p);
-    const int32_t t = p - s;
-    if (s < nS && (t >= nT || a.colind_s[R.sb + s] < int32_t(a.newkey[R.nb + t] & mask))) {
-      sslot = R.sb + s;
-      col = a.colind_s[sslot];
-    } else {
-      nk = R.nb + t;
-      col = int32_t(a.newkey[nk] & mask);
-    }
-  }
-  float K[6] = {0, 0, 0, 0, 0, 0}, F[3] = {0, 0, 0};
-  if (col != i) {
-    const float3 xi = ld3(a.x, i), vi = ld3(a.v, i);
-    const float3 xj = ld3(a.x, col), vj = ld3(a.v, col);
-    const Edge ed = edge_of(xi, xj);
-    const float3 wd = make_float3(vj.x - vi.x, vj.y - vi.y, vj.z - vi.z);
-    if (sslot >= 0) {
-      const int32_t e1 = a.sblk_ptr[sslot + 1];
-      for (int32_t e = a.sblk_ptr[sslot]; e < e1; ++e) {
-        const float2 kl = a.sentry[e];
-        element_terms(ed, wd, a.dt, a.h2, kl.x, kl.y, K, F);
-      }
-    }
-    // contacts on this (row, col) pair: a run of equal sorted keys
-    int32_t t0 = -1;
-    const uint64_t key = (uint64_t(i) << a.B) | uint64_t(col);
-    if (nk >= 0) {
-      t0 = a.newfirst[nk];
-    } else if (R.ee > R.eb) {
-      const int32_t t = lower_bound_key(a.skey, R.eb, R.ee, key);
-      if (t < R.ee && a.skey[t] == key) t0 = t;
-    }
-    if (t0 >= 0) {
-      for (int32_t t = t0; t < m_valid && a.skey[t] == key; ++t) {
-        const int32_t c = a.sval[t];
-        element_terms(ed, wd, a.dt, a.h2, a.ck[c], a.cr[c], K, F);
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kSymBlock; ++t) stv[t] = K[t];
-  stf[0] = F[0]; stf[1] = F[1]; stf[2] = F[2];
-  *stc = col;
-}
-
-// Diagonal block, right-hand side and block-Jacobi inverse of row i from the
-// row's compensated sum h^2 sum K = Ks + Kc (6 unique entries, Kc the
-// TwoSum compensation) and its force sum.  The mass is added to the small
+// Diagonal block (written to the row's diagonal slot dpos), right-hand side
+// and block-Jacobi inverse of row i from the row's compensated sum
+// -sum_j A_ij = h^2 sum K = Ks + Kc over its off-diagonal blocks as stored
+// (6 unique entries, Kc the TwoSum compensation) and its force sum.  The mass is added to the small
 // compensation term first, so the diagonal is rounded once from the exact
 // total: adding m after rounding the large sum would round the same m to the
 // same ulp grid in every row of a binade -- a coherent shift of the mass by
 // ~0.1%, which the soft modes of the system amplify.
-__device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const float (&Ks)[6],
-                                           const float (&Kc)[6], const float (&Fs)[3],
-                                           float (&D)[kSymBlock]) {
+__device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, int64_t dpos,
+                                           const float (&Ks)[6], const float (&Kc)[6],
+                                           const float (&Fs)[3]) {
+  float D[kSymBlock];
   const float m = a.mass[i];
   // packed symmetric diagonal block (d00 d01 d02 d11 d12 d22)
   D[0] = Ks[0] + (Kc[0] + m); D[1] = Ks[1] + Kc[1]; D[2] = Ks[2] + Kc[2];
@@ -379,6 +359,8 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const fl
   a.pinv6[3 * a.vs + i] = c11 * id;
   a.pinv6[4 * a.vs + i] = c12 * id;
   a.pinv6[5 * a.vs + i] = c22 * id;
+#pragma unroll
+  for (int t = 0; t < kSymBlock; ++t) a.vals[kSymBlock * dpos + t] = D[t];
   bool ok = finite3(b0, b1, b2) && isfinite(det) && det > 0.0f;
 #pragma unroll
   for (int t = 0; t < kSymBlock; ++t) ok = ok && isfinite(D[t]);
@@ -387,193 +369,134 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, const fl
 
 // Four CTAs per SM (64 registers a thread): the kernel is bound by the
 // latency of its gathers and of the per-row reductions, so occupancy pays
-// more than the few spills it costs.
-__global__ void __launch_bounds__(kAsmThreads, 4)
+
+// kRowLanes lanes per row.  Lane l takes the row's blocks l, l + kRowLanes,
+// ... in column order: it finds the block's column (the spring pattern and
+// the row's new blocks merged), evaluates every element of the block -- the
+// spring entries of a spring block, then the block's contacts in input
+// order -- writes the block's column and, off the diagonal, its packed
+// value, and adds the negated value and the block's force into its
+// compensated (TwoSum) partial sums.  A butterfly whose steps are
+// commutative merges the lanes' partials (all lanes end with the same
+// bits), and lane 0 forms the diagonal block, b and the block-Jacobi
+// inverse.  Rows are independent: no shared memory and no CTA barrier.
+//
+// Two lanes per row at three CTAs per SM (80 registers) were the fastest of
+// a sweep on the 1.65M-triangle cloth (whole assembly per step): 16 lanes
+// 0.78 ms, 8 lanes 0.58 ms, 4 lanes 0.51 ms (four CTAs per SM), 2 lanes
+// 0.47 ms, 1 lane 0.62 ms; four or more CTAs per SM spill and lose.  Fewer
+// lanes cut the butterfly's and the row finish's share of the
+// instructions; one lane per row leaves each row's loads in a serial chain.
+#ifndef PCLOTH_ASM_CTAS
+#define PCLOTH_ASM_CTAS 3
+#endif
+__global__ void __launch_bounds__(kAsmThreads, PCLOTH_ASM_CTAS)
 assemble_rows(AsmArgs a) {
-  __shared__ RowInfo rows[kAsmRows + 1];
-  __shared__ float stv[kAsmCap * kSymBlock];
-  __shared__ float stf[kAsmCap * 3];
-  __shared__ int32_t stc[kAsmCap];
-  __shared__ double red[9][kAsmThreads / 32];
-  __shared__ double acc[9];
-
-  const int32_t r0 = blockIdx.x * kAsmRows;
-  const int32_t nrows = min(kAsmRows, a.n - r0);
-  const int32_t m_valid = a.has_contacts ? a.counters[1] : 0;
-  const uint64_t mask = (uint64_t(1) << a.B) - 1;
-  (void)mask;
-
-  // ---- phase 1: row bounds, rebuilt row pointers ------------------------
-  if (threadIdx.x <= nrows) {
-    const int32_t ri = threadIdx.x, i = r0 + ri;
-    RowInfo R;
-    R.sb = a.rowptr_s[i];
-    R.se = (ri < nrows) ? a.rowptr_s[i + 1] : R.sb;
-    if (a.has_contacts) {
-      const int32_t nb0 = a.tile_nb[blockIdx.x], nb1 = a.tile_nb[blockIdx.x + 1];
-      const int32_t eb0 = a.tile_eb[blockIdx.x], eb1 = a.tile_eb[blockIdx.x + 1];
-      const uint64_t key = uint64_t(i) << a.B;
-      R.nb = (ri == 0) ? nb0 : (ri == nrows ? nb1 : lower_bound_key(a.newkey, nb0, nb1, key));
-      R.eb = (ri == 0) ? eb0 : (ri == nrows ? eb1 : lower_bound_key(a.skey, eb0, eb1, key));
-    } else {
-      R.nb = 0;
-      R.eb = 0;
-    }
-    R.ob = R.sb + R.nb;
-    rows[ri] = R;
-    if (ri < nrows || i == a.n) a.rowptr[i] = R.ob;
+  const int32_t lane = int32_t(threadIdx.x) % kRowLanes;
+  const int64_t row = (int64_t(blockIdx.x) * kAsmThreads + threadIdx.x) / kRowLanes;
+  const bool live = row < a.n;
+  // lanes past the last row shadow it (same loads, no writes), so that every
+  // lane of the warp takes part in the shuffles
+  const int32_t i = live ? int32_t(row) : a.n - 1;
+  const int32_t sb = a.rowptr_s[i], se = a.rowptr_s[i + 1];
+  int32_t nb = 0, ne = 0, eb = 0, ee = 0;
+  if (a.has_contacts) {
+    nb = a.nbefore[i];
+    ne = a.nbefore[i + 1];
+    eb = a.ebefore[i];
+    ee = a.ebefore[i + 1];
   }
-  __syncthreads();
-  if (threadIdx.x < nrows) {
-    rows[threadIdx.x].ne = rows[threadIdx.x + 1].nb;
-    rows[threadIdx.x].ee = rows[threadIdx.x + 1].eb;
+  const int32_t ob = sb + nb;   // the row's first block in the full pattern
+  const int32_t nS = se - sb, nT = ne - nb, len = nS + nT;
+  if (live && lane == 0) {
+    a.rowptr[i] = ob;
+    if (i == a.n - 1) a.rowptr[a.n] = se + ne;
   }
-  __syncthreads();
-
-  // ---- phase 2..4: groups of whole rows that fit in the staging ---------
-  int32_t g = 0;
-  while (g < nrows) {
-    int32_t e = g + 1;
-    while (e < nrows && rows[e + 1].ob - rows[g].ob <= kAsmCap) ++e;
-    const int32_t gob = rows[g].ob;
-    const int32_t nblk = rows[e].ob - gob;
-    if (nblk <= kAsmCap) {
-      // phase 2: every block of the group, one thread per block
-      for (int32_t o = threadIdx.x; o < nblk; o += kAsmThreads) {
-        // row of block o: last ri in [g, e) with rows[ri].ob <= gob + o
-        int32_t lo = g, hi = e - 1;
-        while (lo < hi) {
-          const int32_t mid = (lo + hi + 1) >> 1;
-          if (rows[mid].ob <= gob + o) lo = mid; else hi = mid - 1;
-        }
-        const RowInfo R = rows[lo];
-        compute_block(a, r0 + lo, R, gob + o - R.ob, &stv[kSymBlock * o], &stf[3 * o], &stc[o],
-                      m_valid);
-      }
-      __syncthreads();
-      // phase 3: eight threads per row (kAsmRows x 8 = kAsmThreads) reduce
-      // its blocks into the diagonal.  h^2 sum K is compensated (TwoSum):
-      // the diagonal is ~h^2 k while the mass it must preserve is far
-      // smaller.  Thread q of a row takes blocks q, q + 8, ... in column
-      // order; the eight (sum, compensation) pairs are then merged by a
-      // butterfly whose steps are commutative, so the order is fixed and
-      // all eight threads hold the same bits.
-      {
-        const int32_t ri = g + int32_t(threadIdx.x) / kRowLanes;
-        const int32_t q = int32_t(threadIdx.x) % kRowLanes;
-        const bool live = ri < e;
-        const int32_t i = r0 + ri;
-        float Ks[6] = {0, 0, 0, 0, 0, 0}, Kc[6] = {0, 0, 0, 0, 0, 0}, Fs[3] = {0, 0, 0};
-        int32_t dpos = -1;
-        if (live) {
-          const int32_t o0 = rows[ri].ob - gob, o1 = rows[ri + 1].ob - gob;
-          for (int32_t o = o0 + q; o < o1; o += kRowLanes) {
-            if (stc[o] == i) { dpos = o; continue; }
-            const float* sv = &stv[kSymBlock * o];
-#pragma unroll
-            for (int t = 0; t < 6; ++t) {
-              const float x = -sv[t];
-              const float sum = Ks[t] + x;
-              const float bp = sum - Ks[t];
-              Kc[t] += (Ks[t] - (sum - bp)) + (x - bp);
-              Ks[t] = sum;
-            }
-            Fs[0] += stf[3 * o]; Fs[1] += stf[3 * o + 1]; Fs[2] += stf[3 * o + 2];
-          }
-        }
-#pragma unroll
-        for (int off = kRowLanes / 2; off > 0; off >>= 1) {
-#pragma unroll
-          for (int t = 0; t < 6; ++t) {
-            const float so = __shfl_xor_sync(0xffffffffu, Ks[t], off);
-            const float co = __shfl_xor_sync(0xffffffffu, Kc[t], off);
-            // TwoSum's error is the exact rounding error of the sum, so
-            // both lanes of the pair get the same bits in either order
-            const float sum = Ks[t] + so;
-            const float bp = sum - Ks[t];
-            const float err = (Ks[t] - (sum - bp)) + (so - bp);
-            Kc[t] = (Kc[t] + co) + err;
-            Ks[t] = sum;
-          }
-#pragma unroll
-          for (int t = 0; t < 3; ++t) Fs[t] += __shfl_xor_sync(0xffffffffu, Fs[t], off);
-          dpos = max(dpos, __shfl_xor_sync(0xffffffffu, dpos, off));
-        }
-        if (live && q == 0) {
-          float D[kSymBlock];
-          finish_row(a, i, Ks, Kc, Fs, D);
-          if (dpos >= 0) {
-#pragma unroll
-            for (int t = 0; t < kSymBlock; ++t) stv[kSymBlock * dpos + t] = D[t];
-          } else {
-            atomicOr(a.status, ST_CAPACITY);  // diagonal missing: cannot happen
-          }
-        }
-      }
-      __syncthreads();
-      // phase 4: coalesced write-out of values and column indices
-      float* dst = a.vals + kSymBlock * int64_t(gob);
-      for (int32_t f = threadIdx.x; f < kSymBlock * nblk; f += kAsmThreads) dst[f] = stv[f];
-      for (int32_t o = threadIdx.x; o < nblk; o += kAsmThreads) a.colind[gob + o] = stc[o];
-      __syncthreads();
+  const float3 xi = ld3(a.x, i), vi = ld3(a.v, i);
+  float Ks[6] = {0, 0, 0, 0, 0, 0}, Kc[6] = {0, 0, 0, 0, 0, 0}, Fs[3] = {0, 0, 0};
+  int32_t dpos = -1;   // position of the diagonal block in the row
+  for (int32_t p = lane; p < len; p += kRowLanes) {
+    int32_t col, sslot = -1, nk = -1;
+    if (nT == 0) {
+      sslot = sb + p;
+      col = a.colind_s[sslot];
     } else {
-      // one row longer than the staging: stream it through in pieces
-      const int32_t ri = g, i = r0 + ri;
-      const RowInfo R = rows[ri];
-      if (threadIdx.x < 9) acc[threadIdx.x] = 0.0;
-      int32_t dpos_abs = -1;
-      for (int32_t c0 = 0; c0 < nblk; c0 += kAsmCap) {
-        const int32_t cn = min(kAsmCap, nblk - c0);
-        __syncthreads();
-        for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads)
-          compute_block(a, i, R, c0 + o, &stv[kSymBlock * o], &stf[3 * o], &stc[o], m_valid);
-        __syncthreads();
-        // fixed-order fp64 partial sums (one row: the cost is negligible):
-        // thread t owns blocks t, t+T, ...
-        double part[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
-        for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads) {
-          if (stc[o] == i) { dpos_abs = gob + c0 + o; continue; }
-          const float* s = &stv[kSymBlock * o];
-          part[0] -= s[0]; part[1] -= s[1]; part[2] -= s[2];
-          part[3] -= s[3]; part[4] -= s[4]; part[5] -= s[5];
-          part[6] += stf[3 * o]; part[7] += stf[3 * o + 1]; part[8] += stf[3 * o + 2];
-        }
-#pragma unroll
-        for (int q = 0; q < 9; ++q) {
-          double vq = part[q];
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) vq += __shfl_down_sync(0xffffffffu, vq, off);
-          if ((threadIdx.x & 31) == 0) red[q][threadIdx.x >> 5] = vq;
-        }
-        __syncthreads();
-        if (threadIdx.x < 9) {
-          double s = 0.0;
-          for (int w = 0; w < kAsmThreads / 32; ++w) s += red[threadIdx.x][w];
-          acc[threadIdx.x] += s;
-        }
-        float* dst = a.vals + kSymBlock * (int64_t(gob) + c0);
-        for (int32_t f = threadIdx.x; f < kSymBlock * cn; f += kAsmThreads) dst[f] = stv[f];
-        for (int32_t o = threadIdx.x; o < cn; o += kAsmThreads) a.colind[gob + c0 + o] = stc[o];
+      const int32_t* S = a.colind_s + sb;
+      const int32_t* T = a.newcol + eb;
+      const int32_t s = merge_split(S, nS, T, nT, p);
+      const int32_t t = p - s;
+      if (s < nS && (t >= nT || S[s] < T[t])) {
+        sslot = sb + s;
+        col = S[s];
+      } else {
+        nk = t;
+        col = T[t];
       }
-      __syncthreads();
-      // the thread that saw the diagonal writes it (exactly one does)
-      if (dpos_abs >= 0) {
-        float Ks[6], Kc[6];
-#pragma unroll
-        for (int t = 0; t < 6; ++t) {   // exact split of the fp64 sum into hi + lo
-          Ks[t] = float(acc[t]);
-          Kc[t] = float(acc[t] - double(Ks[t]));
-        }
-        const float Fs[3] = {float(acc[6]), float(acc[7]), float(acc[8])};
-        float D[kSymBlock];
-        finish_row(a, i, Ks, Kc, Fs, D);
-        float* dst = a.vals + kSymBlock * int64_t(dpos_abs);
-#pragma unroll
-        for (int t = 0; t < kSymBlock; ++t) dst[t] = D[t];
-      }
-      __syncthreads();
     }
-    g = e;
+    if (live) a.colind[ob + p] = col;
+    if (col == i) {
+      dpos = p;
+      continue;
+    }
+    float K[6] = {0, 0, 0, 0, 0, 0}, F[3] = {0, 0, 0};
+    const float3 xj = ld3(a.x, col), vj = ld3(a.v, col);
+    const Edge ed = edge_of(xi, xj);
+    const float3 wd = make_float3(vj.x - vi.x, vj.y - vi.y, vj.z - vi.z);
+    if (sslot >= 0) {
+      const int32_t e1 = a.sblk_ptr[sslot + 1];
+      for (int32_t e = a.sblk_ptr[sslot]; e < e1; ++e) {
+        const float2 kl = a.sentry[e];
+        element_terms(ed, wd, a.dt, a.h2, kl.x, kl.y, K, F);
+      }
+    }
+    // the block's contacts: a run of entries with this column
+    int32_t t0 = ee;
+    if (nk >= 0)
+      t0 = a.newfirst[eb + nk];
+    else if (ee > eb)
+      t0 = lower_bound_col(a.centry, eb, ee, col);
+    for (int32_t t = t0; t < ee; ++t) {
+      const uint64_t en = a.centry[t];
+      if (int32_t(en >> 32) != col) break;
+      const int32_t c = int32_t(uint32_t(en));
+      element_terms(ed, wd, a.dt, a.h2, a.ck[c], a.cr[c], K, F);
+    }
+    if (live) {
+      float* dst = a.vals + kSymBlock * (int64_t(ob) + p);
+#pragma unroll
+      for (int t = 0; t < kSymBlock; ++t) dst[t] = K[t];
+    }
+    // the diagonal takes -(the block as stored), so that the rows of A sum
+    // to M up to the compensated sums' own error
+#pragma unroll
+    for (int t = 0; t < 6; ++t) add_comp(Ks[t], Kc[t], -K[t]);
+    Fs[0] += F[0];
+    Fs[1] += F[1];
+    Fs[2] += F[2];
+  }
+  // merge the lanes' partials: TwoSum's error is the exact rounding error of
+  // the sum, so both lanes of a pair get the same bits in either order
+#pragma unroll
+  for (int off = kRowLanes / 2; off > 0; off >>= 1) {
+#pragma unroll
+    for (int t = 0; t < 6; ++t) {
+      const float so = __shfl_xor_sync(0xffffffffu, Ks[t], off);
+      const float co = __shfl_xor_sync(0xffffffffu, Kc[t], off);
+      const float sum = Ks[t] + so;
+      const float bp = sum - Ks[t];
+      const float err = (Ks[t] - (sum - bp)) + (so - bp);
+      Kc[t] = (Kc[t] + co) + err;
+      Ks[t] = sum;
+    }
+#pragma unroll
+    for (int t = 0; t < 3; ++t) Fs[t] += __shfl_xor_sync(0xffffffffu, Fs[t], off);
+    dpos = max(dpos, __shfl_xor_sync(0xffffffffu, dpos, off));
+  }
+  if (live && lane == 0) {
+    if (dpos >= 0)
+      finish_row(a, i, int64_t(ob) + dpos, Ks, Kc, Fs);
+    else
+      atomicOr(a.status, ST_CAPACITY);   // diagonal missing: cannot happen
   }
 }
 
@@ -616,45 +539,44 @@ int launch_pinv_expand(Handle* h, float* out9) {
   return check_launch(h, "pinv expand");
 }
 
+
 int assemble_system(Handle* h, const float* x, const float* v,
                     const pcloth_springs* contacts, float dt) {
   const int32_t nc = contacts ? contacts->n : 0;
-  const int B = h->key_bits;
-  const int32_t ntiles = (h->n + kAsmRows - 1) / kAsmRows;
+  const int32_t n = h->n;
   cudaStream_t s = h->stream;
   h->bell_valid = false;   // the pattern changes below
   if (h->prof.on) cudaEventRecord(h->ev[0], s);
-  int rc = PCLOTH_OK;
   AsmArgs a{};
   a.has_contacts = nc > 0;
   if (nc > 0) {
-    const int32_t m = 2 * nc;
-    contact_keys<<<(nc + 255) / 256, 256, 0, s>>>(nc, h->n, B, contacts->i, contacts->j,
-                                                   contacts->k, contacts->rest, h->ckey[0],
-                                                   h->cval[0], h->d_status);
-    cudaMemsetAsync(h->counters, 0, 4 * sizeof(int32_t), s);
+    int32_t* rowcnt = h->rowcnt;          // [n+1]: counts, then first entry per row
+    int32_t* fill = h->rowcnt + (n + 1);  // [n+1]: scatter cursors
+    uint64_t* centry = h->ckey[0];
+    cudaError_t e = cudaMemsetAsync(h->rowcnt, 0, 2 * (size_t(n) + 1) * sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "contact counts reset");
+    const int cgrid = (nc + 255) / 256, rgrid = (n + 1 + 255) / 256;
+    contact_count<<<cgrid, 256, 0, s>>>(nc, n, contacts->i, contacts->j, contacts->k,
+                                        contacts->rest, rowcnt, h->d_status);
     h->launches += 1;
-    int cur = radix_sort_pairs(h, h->ckey, h->cval, m, 2 * B);
-    if (cur < 0) return cur;
-    contact_classify<<<(m + 255) / 256, 256, 0, s>>>(m, B, h->ckey[cur], h->rowptr_s,
-                                                     h->colind_s, h->flags, h->counters);
-    h->launches += 1;
-    rc = scan_exclusive(h, h->flags, m, h->counters);
+    int rc = scan_exclusive(h, rowcnt, n + 1, h->counters + 1);
     if (rc != PCLOTH_OK) return rc;
-    contact_compact<<<(m + 255) / 256, 256, 0, s>>>(m, h->ckey[cur], h->flags, h->counters,
-                                                    h->newkey, h->newfirst);
-    h->launches += 1;
-    a.skey = h->ckey[cur];
-    a.sval = h->cval[cur];
+    contact_scatter<<<cgrid, 256, 0, s>>>(nc, n, contacts->i, contacts->j, rowcnt, fill,
+                                          centry);
+    row_classify<<<rgrid, 256, 0, s>>>(n, rowcnt, centry, h->rowptr_s, h->colind_s, h->newcol,
+                                       h->newfirst, h->newcnt);
+    h->launches += 2;
+    rc = scan_exclusive(h, h->newcnt, n + 1, h->counters);
+    if (rc != PCLOTH_OK) return rc;
+    a.ebefore = rowcnt;
+    a.nbefore = h->newcnt;
+    a.centry = centry;
+    a.newcol = h->newcol;
+    a.newfirst = h->newfirst;
     a.ck = contacts->k;
     a.cr = contacts->rest;
   }
-  tile_bounds<<<(ntiles + 1 + 255) / 256, 256, 0, s>>>(ntiles, h->n, B, nc > 0, h->newkey,
-                                                        a.skey, h->counters, h->tile_nb,
-                                                        h->tile_eb);
-  h->launches += 1;
-  a.n = h->n;
-  a.B = B;
+  a.n = n;
   a.dt = dt;
   a.h2 = dt * dt;
   a.gx = h->gravity[0];
@@ -667,11 +589,6 @@ int assemble_system(Handle* h, const float* x, const float* v,
   a.colind_s = h->colind_s;
   a.sblk_ptr = h->sblk_ptr;
   a.sentry = h->sentry;
-  a.newkey = h->newkey;
-  a.newfirst = h->newfirst;
-  a.tile_nb = h->tile_nb;
-  a.tile_eb = h->tile_eb;
-  a.counters = h->counters;
   a.rowptr = h->rowptr;
   a.colind = h->colind;
   a.vals = h->vals;
@@ -679,7 +596,8 @@ int assemble_system(Handle* h, const float* x, const float* v,
   a.pinv6 = h->pinv6;
   a.vs = h->vstride;
   a.status = h->d_status;
-  assemble_rows<<<ntiles, kAsmThreads, 0, s>>>(a);
+  const int64_t rows_per_cta = kAsmThreads / kRowLanes;
+  assemble_rows<<<unsigned((n + rows_per_cta - 1) / rows_per_cta), kAsmThreads, 0, s>>>(a);
   h->launches += 1;
   if (h->prof.on) {
     cudaEventRecord(h->ev[1], s);

@@ -602,9 +602,11 @@ int loop_attrs(int device) {
   constexpr size_t smem = Pipe<BW>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(pcg_loop<BW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(smem));
+  cudaFuncAttributes fa{};
+  if (PCLOTH_PIPE_CARVE && e == cudaSuccess) e = cudaFuncGetAttributes(&fa, pcg_loop<BW>);
   if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
     e = cudaFuncSetAttribute(pcg_loop<BW>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             pipe_carveout_percent(smem));
+                             pipe_carveout_percent(smem, fa.sharedSizeBytes));
   if (e != cudaSuccess) return int(e);
   if (device >= 0 && device < 64) g_loop_attr[w][device] = true;
   return 0;
@@ -625,13 +627,23 @@ int loop_grid_for(int32_t n, int device, int sm_count, int* grid) {
   return 0;
 }
 
-// Enqueues the persistent solve (cooperative launch) on `stream`.
+// Enqueues the persistent solve (cooperative launch) on `stream`.  Should the
+// device refuse to hold the whole grid at once (the occupancy estimate and
+// the launch disagree), the grid is halved until it fits -- any grid is
+// correct, each CTA then walks more tiles -- and *grid keeps the size that
+// launched.
 template <int BW>
-cudaError_t launch_loop(const LoopArgs& a, int grid, cudaStream_t stream) {
+cudaError_t launch_loop(const LoopArgs& a, int* grid, cudaStream_t stream) {
   LoopArgs args = a;
   void* params[] = {&args};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(pcg_loop<BW>), dim3(grid),
-                                     dim3(kPipeThreads), params, Pipe<BW>::kSmem, stream);
+  while (true) {
+    const cudaError_t e = cudaLaunchCooperativeKernel(
+        reinterpret_cast<const void*>(pcg_loop<BW>), dim3(*grid), dim3(kPipeThreads), params,
+        Pipe<BW>::kSmem, stream);
+    if (e != cudaErrorCooperativeLaunchTooLarge || *grid <= 1) return e;
+    cudaGetLastError();   // a launch-configuration error: not sticky
+    *grid = (*grid + 1) / 2;
+  }
 }
 
 // Self-tests of the bounded waits: each kernel waits, with a short limit, on
@@ -743,8 +755,8 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
   cudaError_t e = cudaMemsetAsync(h->bar, 0, sizeof(unsigned long long), s);
   if (e != cudaSuccess) return cuda_fail(h, e, "pcg barrier reset");
   if (prof) cudaEventRecord(h->ev[2], s);
-  e = h->blk == kSymBlock ? launch_loop<kSymBlock>(a, h->loop_grid, s)
-                          : launch_loop<9>(a, h->loop_grid, s);
+  e = h->blk == kSymBlock ? launch_loop<kSymBlock>(a, &h->loop_grid, s)
+                          : launch_loop<9>(a, &h->loop_grid, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "pcg launch");
   h->launches += 1;
   if (prof) cudaEventRecord(h->ev[3], s);
@@ -967,7 +979,7 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
   bsr3_diag_inverse<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, vals, pinv6,
                                                         kStaticPlane, status);
   e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_loop<9>(a, grid, stream);
+  if (e == cudaSuccess) e = launch_loop<9>(a, &grid, stream);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve launch");
   PcgState st{};
   e = cudaMemcpyAsync(&st, a.state, sizeof(PcgState), cudaMemcpyDeviceToHost, stream);

@@ -45,9 +45,7 @@ constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;
 
 constexpr int kSymBlock = 6;   // floats per packed symmetric 3x3 block
-constexpr int kAsmRows = 32;      // rows per assembly tile
-constexpr int kAsmCap = 768;      // blocks staged per assembly group
-constexpr int kAsmThreads = 256;
+constexpr int kAsmThreads = 256;  // threads per CTA of the row assembly
 
 // Rows of A longer than this many blocks are summed with compensation
 // (TwoSum) in every product A x: the plain fp32 sum of n products errs by up
@@ -113,22 +111,20 @@ struct Handle {
   float* rhs = nullptr;          // 3n
   float* pinv6 = nullptr;        // [6][vstride] planes P00 P01 P02 P11 P12 P22
 
-  // per-step contact workspace (capacity 2*max_contacts entries)
+  // per-step contact workspace (capacity 2*max_contacts entries).  The
+  // assembly buckets a step's contact entries by row: ckey[0] holds them,
+  // per row sorted by (column << 32 | contact id); ckey/cval are also the
+  // radix sort's buffers for contact finding.
   uint64_t* ckey[2] = {nullptr, nullptr};
   int32_t* cval[2] = {nullptr, nullptr};
   int32_t* sort_counts = nullptr;  // radix * tiles
-  int32_t* flags = nullptr;        // new-block flags, then their prefix
   int32_t* scan_tmp = nullptr;     // per-tile sums
-  uint64_t* newkey = nullptr;      // keys of new blocks (sorted)
-  int32_t* newfirst = nullptr;     // first sorted entry of each new block
-  int32_t* tile_nb = nullptr;      // per assembly tile: first new block
-  int32_t* tile_eb = nullptr;      // per assembly tile: first contact entry
-  int32_t* counters = nullptr;     // [0] = #new blocks, [1] = #valid entries
-  const uint64_t* skey = nullptr;  // sorted keys of the current step
-  const int32_t* sval = nullptr;   // their contact ids
-  const float* ck = nullptr;       // contact stiffness (caller memory)
-  const float* cr = nullptr;       // contact rest length (caller memory)
-  int32_t nc = 0;
+  int32_t* rowcnt = nullptr;       // [2(n+1)]: entries per row, scanned to the first
+                                   // entry of each row; then the scatter cursors
+  int32_t* newcnt = nullptr;       // [n+1]: new blocks per row, scanned to those before it
+  int32_t* newcol = nullptr;       // a row's new columns, at its first entry's index
+  int32_t* newfirst = nullptr;     // first entry of each new column
+  int32_t* counters = nullptr;     // [0] = #new blocks, [1] = #valid entries, [2] pairs
 
   // host-input staging for pcloth_step_host
   float* hx = nullptr;
@@ -197,7 +193,7 @@ int assemble_system(Handle* h, const float* x, const float* v,
 
 // spmv.cu
 int spmv_grid_for(int32_t n, int sm_count);
-int pipe_carveout_percent(size_t smem);
+int pipe_carveout_percent(size_t dyn_smem, size_t static_smem);
 int launch_spmv(Handle* h, const float* in, float* out);
 
 // contacts.cu: vertex-vertex proximity contacts by spatial hashing

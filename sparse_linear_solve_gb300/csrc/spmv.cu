@@ -64,12 +64,17 @@ bool g_attr_done[64] = {};
 }  // namespace
 
 // Shared-memory carveout: just enough for kPipeCtasPerSm CTAs, so that the
-// rest of the unified L1/shared storage stays L1 cache for the gathers.
-int pipe_carveout_percent(size_t smem) {
-  const size_t need = size_t(kPipeCtasPerSm) * (smem + 2048);
-  const size_t max_smem = 228 * 1024;
-  int pct = int((need * 100 + max_smem - 1) / max_smem);
-  return pct > 100 ? 100 : pct;
+// rest of the unified L1/shared storage stays L1 cache for the gathers.  A
+// CTA takes its dynamic and static shared memory plus the 1 KB the runtime
+// reserves per CTA; the carveout is the smallest shared-memory capacity the
+// SM offers that holds that many CTAs (a hint that rounded down would leave
+// room for fewer CTAs than a cooperative launch of the full grid needs).
+int pipe_carveout_percent(size_t dyn_smem, size_t static_smem) {
+  const size_t need = size_t(kPipeCtasPerSm) * (dyn_smem + static_smem + 1024);
+  static const int kCapsKb[] = {0, 8, 16, 32, 64, 100, 132, 164, 196, 228};
+  for (int c : kCapsKb)
+    if (size_t(c) * 1024 >= need) return (c * 100 + 227) / 228;
+  return 100;
 }
 
 int spmv_grid_for(int32_t n, int sm_count) {
@@ -83,10 +88,12 @@ int launch_spmv(Handle* h, const float* in, float* out) {
   if (!(h->device >= 0 && h->device < 64 && g_attr_done[h->device])) {
     cudaError_t e = cudaFuncSetAttribute(spmv_plain<kSymBlock>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaFuncAttributes fa{};
+    if (PCLOTH_PIPE_CARVE && e == cudaSuccess) e = cudaFuncGetAttributes(&fa, spmv_plain<kSymBlock>);
     if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
       e = cudaFuncSetAttribute(spmv_plain<kSymBlock>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
-                               pipe_carveout_percent(smem));
+                               pipe_carveout_percent(smem, fa.sharedSizeBytes));
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(spmv)");
     if (h->device >= 0 && h->device < 64) g_attr_done[h->device] = true;
   }
