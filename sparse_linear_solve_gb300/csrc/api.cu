@@ -33,12 +33,12 @@ void free_handle(Handle* h) {
   cudaSetDevice(h->device);
   cudaStreamSynchronize(h->stream);
   void* bufs[] = {h->mass, h->rowptr_s, h->colind_s, h->sblk_ptr, h->sentry,
-                  h->rowptr, h->colind, h->vals, h->rhs, h->pinv6,
+                  h->rowptr, h->colind, h->vals, h->rhs, h->vec_arena,
                   h->ckey[0], h->ckey[1], h->cval[0], h->cval[1],
                   h->sort_counts, h->scan_tmp, h->rowcnt, h->newcnt, h->newcol,
                   h->newfirst, h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
-                  h->dv, h->dv3, h->r3, h->z3, h->p4, h->q3, h->rec, h->bar,
+                  h->dv, h->rec, h->bar,
                   h->phase_ns, h->state, h->d_status, h->bell_wmax, h->bell_col, h->bell_val,
                   h->vkey[0], h->vkey[1], h->vid[0], h->vid[1]};
   for (void* b : bufs)
@@ -229,7 +229,35 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->rhs, 3 * n + vpad));
   h->vstride = (n + 31) / 32 * 32;
   const int64_t vs = h->vstride;
-  A(dalloc(&h->pinv6, 6 * vs + vpad));
+  {
+    // The vectors of the PCG's row phases in one allocation, each array on
+    // its own 2 MB boundary plus a stagger of kVecStagger bytes times its
+    // index, so that the streams a phase reads at the same row index do not
+    // all sit at the same offset within their pages.
+    const size_t sizes[6] = {size_t(n + vpad) * sizeof(float4),           // p
+                             size_t(3 * vs + vpad) * sizeof(float),       // q
+                             size_t(3 * vs + vpad) * sizeof(float),       // r
+                             size_t(3 * vs + vpad) * sizeof(float),       // z
+                             size_t(3 * vs + vpad) * sizeof(float),       // dv
+                             size_t(6 * vs + vpad) * sizeof(float)};      // P
+    constexpr size_t kPage = size_t(2) << 20;
+    size_t off[6], cursor = 0;
+    for (int k = 0; k < 6; ++k) {
+      off[k] = (cursor + kPage - 1) / kPage * kPage + size_t(k) * kVecStagger;
+      cursor = off[k] + sizes[k];
+    }
+    unsigned char* base = nullptr;
+    A(cudaMalloc(reinterpret_cast<void**>(&base), cursor));
+    h->vec_arena = base;
+    if (base) {
+      h->p4 = reinterpret_cast<float4*>(base + off[0]);
+      h->q3 = reinterpret_cast<float*>(base + off[1]);
+      h->r3 = reinterpret_cast<float*>(base + off[2]);
+      h->z3 = reinterpret_cast<float*>(base + off[3]);
+      h->dv3 = reinterpret_cast<float*>(base + off[4]);
+      h->pinv6 = reinterpret_cast<float*>(base + off[5]);
+    }
+  }
   for (int b = 0; b < 2; ++b) {
     A(dalloc(&h->ckey[b], ent2));
     A(dalloc(&h->cval[b], ent2));
@@ -250,11 +278,6 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->hck, std::max<int64_t>(mc, 1)));
   A(dalloc(&h->hcr, std::max<int64_t>(mc, 1)));
   A(dalloc(&h->dv, 3 * n + vpad));
-  A(dalloc(&h->dv3, 3 * vs + vpad));
-  A(dalloc(&h->r3, 3 * vs + vpad));
-  A(dalloc(&h->z3, 3 * vs + vpad));
-  A(dalloc(&h->q3, 3 * vs + vpad));
-  A(dalloc(&h->p4, n + vpad));
   A(dalloc(&h->rec, int64_t(h->loop_grid) * kRecSlots));
   A(dalloc(&h->bar, 1));
   A(dalloc(&h->phase_ns, 4));

@@ -58,6 +58,16 @@ constexpr int kAsmThreads = 256;  // threads per CTA of the row assembly
 constexpr int kCompRow = 32;
 
 constexpr int kVecThreads = 256;
+// Bytes by which the PCG's row vectors are staggered past their 2 MB
+// boundaries (array k at k times this), see pcloth_create.  Measured per
+// PCG iteration on the 1.65M-triangle cloth: separate allocations 67.7 us;
+// one arena with staggers of 0, 4, 16, 32, 64, 96, 128, 256 KB, 1 and 1.5 MB
+// gave 66.7, 66.7, 66.35, 66.6, 66.4, 66.7, 66.8, 67.5, 68.2 and 68.4 us (the
+// vector phases move with it: 15.5 us at 64 KB, 17.1 us at 1.5 MB).
+#ifndef PCLOTH_VEC_STAGGER
+#define PCLOTH_VEC_STAGGER 65536
+#endif
+constexpr size_t kVecStagger = PCLOTH_VEC_STAGGER;
 // Per-CTA partial sums of the PCG dot products, one double-float (float2)
 // per slot: p.q, r.z, r.r, b.b.
 constexpr int kRecSlots = 4;
@@ -139,6 +149,7 @@ struct Handle {
   // that are only read and written row by row are three planes (x, y, z) of
   // vstride floats each, so that a warp's loads and stores cover whole
   // sectors and move no padding.
+  void* vec_arena = nullptr;       // one allocation holding p, q, r, z, dv and P
   float* dv = nullptr;             // float[n][3] scratch (pcloth_step without dv)
   int64_t vstride = 0;             // floats per plane: n rounded up to 32
   float* dv3 = nullptr;            // [3][vstride]
