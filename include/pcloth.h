@@ -169,6 +169,36 @@ int pcloth_spmv_bell(pcloth_t h, const float* in, float* out);
 int pcloth_solve(pcloth_t h, double tol, int32_t maxit, float* dv,
                  int32_t* iterations, double* rel_residual);
 
+/* pcloth_solve from an initial iterate: dv (device float32[n][3]) holds the
+ * guess on entry and the solution on return.  The iteration starts from
+ * r = b - A dv, z = P r, p = z (the textbook PCG with a nonzero first
+ * iterate; Sec. 3.1 / Eq. (3)); the stop test is the same, |r|_2 <= tol |b|_2
+ * on the recursive residual, and a guess that already meets it returns after
+ * 0 iterations with *rel_residual = |b - A dv| / |b|.  b = 0 gives dv = 0.
+ * Costs one extra SpMV pass.  Synchronises at the end. */
+int pcloth_solve_guess(pcloth_t h, double tol, int32_t maxit, float* dv,
+                       int32_t* iterations, double* rel_residual);
+
+/* pcloth_step with no host synchronisation and no host-side read, so that a
+ * caller can capture it in a CUDA graph (with the handle's stream set to the
+ * capturing stream) and replay it: it enqueues the assembly, the solve and
+ * the state update on the handle's stream and returns.  The solve's
+ * iterations, residual and status stay on the device until
+ * pcloth_step_result reads them.  Pointers (x, v, dv and the contacts'
+ * arrays) are baked into a captured graph: to replay it for another step,
+ * write that step's contacts into the same arrays (contacts->n is captured
+ * too).  dv may be NULL (library scratch).  Profiling must be off
+ * (PCLOTH_ERR_STATE otherwise: it synchronises).  Errors found on the host
+ * (arguments, contact count) are returned at once. */
+int pcloth_step_async(pcloth_t h, float* x, float* v, const pcloth_springs* contacts,
+                      float dt, double tol, int32_t maxit, float* dv);
+
+/* The outcome of the last solve enqueued by pcloth_step_async: waits for the
+ * handle's stream, writes *iterations and *rel_residual (either may be NULL)
+ * and returns the solve's code (PCLOTH_OK, PCLOTH_NOT_CONVERGED or an error,
+ * as pcloth_step would have).  Synchronises. */
+int pcloth_step_result(pcloth_t h, int32_t* iterations, double* rel_residual);
+
 /* One whole implicit step: assemble at (x, v), solve, then update the state
  * in place: v += dv, x += dt v (Eq. (3) with backward Euler).  x, v device
  * float32[n][3]; dv may be NULL (library scratch is used).  Synchronises. */

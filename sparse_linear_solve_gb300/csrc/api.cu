@@ -398,6 +398,40 @@ int pcloth_solve(pcloth_t ht, double tol, int32_t maxit, float* dv,
   return pcg_solve(h, tol, maxit, dv, iterations, rel_residual);
 }
 
+int pcloth_solve_guess(pcloth_t ht, double tol, int32_t maxit, float* dv,
+                       int32_t* iterations, double* rel_residual) {
+  Handle* h = reinterpret_cast<Handle*>(ht);
+  if (!h) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "NULL handle");
+  if (!dv || maxit < 0 || !(tol >= 0.0))
+    return fail(h, PCLOTH_ERR_INVALID_ARG, "bad dv, tol or maxit");
+  if (!h->assembled) return fail(h, PCLOTH_ERR_STATE, "solve before assemble");
+  cudaSetDevice(h->device);
+  return pcg_solve(h, tol, maxit, dv, iterations, rel_residual, dv, false);
+}
+
+int pcloth_step_async(pcloth_t ht, float* x, float* v, const pcloth_springs* contacts,
+                      float dt, double tol, int32_t maxit, float* dv) {
+  Handle* h = reinterpret_cast<Handle*>(ht);
+  if (!h) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "NULL handle");
+  if (h->prof.on)
+    return fail(h, PCLOTH_ERR_STATE,
+                "profiling synchronises: turn it off for the asynchronous step");
+  if (maxit < 0 || !(tol >= 0.0)) return fail(h, PCLOTH_ERR_INVALID_ARG, "bad tol or maxit");
+  int rc = pcloth_assemble(ht, x, v, contacts, dt);
+  if (rc != PCLOTH_OK) return rc;
+  float* d = dv ? dv : h->dv;
+  rc = pcg_solve(h, tol, maxit, d, nullptr, nullptr, nullptr, true);
+  if (rc != PCLOTH_OK) return rc;
+  return launch_state_update(h, x, v, d, dt);
+}
+
+int pcloth_step_result(pcloth_t ht, int32_t* iterations, double* rel_residual) {
+  Handle* h = reinterpret_cast<Handle*>(ht);
+  if (!h) return fail(nullptr, PCLOTH_ERR_INVALID_ARG, "NULL handle");
+  cudaSetDevice(h->device);
+  return pcg_result(h, iterations, rel_residual);
+}
+
 int pcloth_step(pcloth_t ht, float* x, float* v, const pcloth_springs* contacts,
                 float dt, double tol, int32_t maxit, float* dv,
                 int32_t* iterations, double* rel_residual) {

@@ -188,6 +188,7 @@ struct LoopArgs {
   PcgState* state;
   uint32_t* status;
   float* dv_out;           // caller's float[n][3]
+  const float* x0;         // caller's float[n][3] initial guess (the kGuess kernel only)
   unsigned long long* phase_ns;  // [4] = S, U, P nanoseconds, timed SpMV phases (or null)
   double tol2;
   int32_t maxit;
@@ -232,7 +233,132 @@ struct Lead {
   double rz_old, bbd, rr_last;
 };
 
+// Start of a solve from the caller's guess x0 (P-Cloth Sec. 3.1's PCG with a
+// nonzero first iterate): dv = x0, r = b - A x0 (one SpMV pass of the same
+// pipeline), z = P r, p = z.  A guess that already meets |r| <= tol |b|
+// stops with 0 iterations (and b = 0 gives dv = 0, whatever the guess).
+// Returns whether the iteration runs; every CTA takes the same decision from
+// the same records.  *stop_sh and *zero_sh are the CTA's shared flags.
 template <int BW>
+__device__ __forceinline__ bool start_from_guess(const LoopArgs& a, const PipeMatrix& m,
+                                                 const PipeShared& sh, Consumer& C, Lead& L,
+                                                 int32_t n, int32_t nslots, float2* my_rec,
+                                                 float2* red_sh, int* ok_sh, int* fail_sh,
+                                                 int* stop_sh, int* zero_sh) {
+  const int32_t tid = threadIdx.x;
+  // p = x0 (the SpMV below gathers it), dv = x0
+  for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+    const int32_t i = own_row(f);
+    if (i >= n) continue;
+    const float3 x = make_float3(a.x0[3 * int64_t(i)], a.x0[3 * int64_t(i) + 1],
+                                 a.x0[3 * int64_t(i) + 2]);
+    a.p[i] = make_float4(x.x, x.y, x.z, 0.f);
+    st3(a.dv, a.vs, i, x);
+  }
+  if (!grid_barrier(a.bar, L.epoch, fail_sh, ok_sh)) return false;
+  // q = A x0: one pass of the streaming product
+  if (tid < 32) {
+    if (tid == 0) {
+      Producer P = L.P;
+      if (!producer_pass<BW>(P, sh, m)) timed_out(a.status, fail_sh);
+      L.P = P;
+    }
+  } else {
+    const Vec vm = vec_access();
+    PGather g{a.p, vm};
+    PEpi e{a.p, a.q, a.vs, vm, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+    if (!consumer_pass<BW>(C, sh, g, e)) timed_out(a.status, fail_sh);
+  }
+  __syncthreads();   // this CTA's rows of q are written
+  // r = b - A x0, z = P r; partials r.z, b.b, r.r
+  {
+    float rz = 0.f, bb = 0.f, rr = 0.f;
+    for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+      const int32_t i = own_row(f);
+      if (i >= n) continue;
+      const float3 bv = make_float3(a.b[3 * int64_t(i)], a.b[3 * int64_t(i) + 1],
+                                    a.b[3 * int64_t(i) + 2]);
+      const float3 qv = ld3(a.q, a.vs, i);
+      const float3 rv = make_float3(bv.x - qv.x, bv.y - qv.y, bv.z - qv.z);
+      const float3 zv = apply_p(ld_sym(a.pinv, a.vs, i), rv);
+      st3(a.r, a.vs, i, rv);
+      st3(a.z, a.vs, i, zv);
+      rz += dot3(rv, zv);
+      bb += dot3(bv, bv);
+      rr += dot3(rv, rv);
+    }
+    Dfloat v[2] = {df_of(rz), df_of(bb)};
+    block_sum_df0<kPipeThreads, 2>(v, red_sh);
+    if (tid == 0) {
+      my_rec[REC_RZ] = df_pack(v[0]);
+      my_rec[REC_BB] = df_pack(v[1]);
+    }
+    __syncthreads();
+    Dfloat w[1] = {df_of(rr)};
+    block_sum_df0<kPipeThreads, 1>(w, red_sh);
+    if (tid == 0) my_rec[REC_RR] = df_pack(w[0]);
+  }
+  if (!grid_barrier(a.bar, L.epoch, fail_sh, ok_sh)) return false;
+  {
+    Dfloat rzrr[2], bb[1];
+    records_share<2>(a.rec, gridDim.x, REC_RZ, kPipeThreads, rzrr);
+    records_share<1>(a.rec, gridDim.x, REC_BB, kPipeThreads, bb);
+    Dfloat v[2] = {rzrr[0], bb[0]};
+    block_sum_df0<kPipeThreads, 2>(v, red_sh);
+    if (tid == 0) {
+      L.rz_old = df_value(v[0]);
+      L.bbd = df_value(v[1]);
+    }
+    __syncthreads();
+    Dfloat w[1] = {rzrr[1]};
+    block_sum_df0<kPipeThreads, 1>(w, red_sh);
+    if (tid == 0) {
+      const double rzd = L.rz_old, bbd = L.bbd, rrd = df_value(w[0]);
+      L.rr_last = rrd;
+      int stop = 1;
+      PcgState st{1, 0, PCLOTH_OK, 0, 0.0, sqrt(bbd)};
+      if (!isfinite(bbd) || !isfinite(rrd) || !isfinite(rzd)) {
+        st.code = PCLOTH_ERR_NONFINITE;
+        if (blockIdx.x == 0) atomicOr(a.status, ST_NONFINITE);
+      } else if (!(bbd > 0.0)) {
+        *zero_sh = 1;                      // b = 0: dv = 0 is exact
+      } else {
+        st.relres = sqrt(rrd / bbd);
+        if (rrd <= a.tol2 * bbd)
+          st.code = PCLOTH_OK;             // the guess already meets the tolerance
+        else if (a.maxit <= 0)
+          st.code = PCLOTH_NOT_CONVERGED;
+        else
+          stop = 0;
+      }
+      if (stop && blockIdx.x == 0) *a.state = st;
+      *stop_sh = stop;
+    }
+    __syncthreads();
+  }
+  if (*stop_sh) return false;
+  // p = z; the loop's first product gathers it only after the next barrier
+  for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+    const int32_t i = own_row(f);
+    if (i >= n) continue;
+    const float3 zv = ld3(a.z, a.vs, i);
+    a.p[i] = make_float4(zv.x, zv.y, zv.z, 0.f);
+  }
+  if (!grid_barrier(a.bar, L.epoch, fail_sh, ok_sh)) return false;
+  if (tid == 0) {   // the first stages of the first SpMV
+    Producer P = L.P;
+    for (int j = 0; j < kPipeStages && !P.ended; ++j)
+      if (producer_step<BW>(P, sh, m) < 0) timed_out(a.status, fail_sh);
+    L.P = P;
+  }
+  __syncthreads();
+  return true;
+}
+
+// kGuess: the solve starts from the caller's guess x0 instead of 0 -- one
+// extra SpMV pass and two extra grid barriers before the loop; the loop
+// itself is the same code.
+template <int BW, bool kGuess>
 __global__ void __launch_bounds__(kPipeThreads, kPipeCtasPerSm)
 pcg_loop(LoopArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -242,6 +368,7 @@ pcg_loop(LoopArgs a) {
   __shared__ int fail_sh;   // a wait of this CTA timed out
   __shared__ int stop_sh;
   __shared__ float scal_sh;
+  __shared__ int zero_sh;   // b = 0: dv = 0 is exact, whatever the guess
   __shared__ Lead L;
   // every SpMV pass walks the same tiles: their block ranges, once
   __shared__ int2 tb_sh[kTileCache];
@@ -261,73 +388,80 @@ pcg_loop(LoopArgs a) {
   Consumer C;
   if (tid == 0) {
     fail_sh = 0;
+    zero_sh = 0;
     producer_begin(L.P, m);
     L.epoch = L.t_s = L.t_u = L.t_p = L.n_timed = L.t_prev = 0;
   }
   consumer_begin(C);
 
-  // ---- init: r = b, z = P b, dv = 0, p = z; partials r.z and b.b ---------
-  {
-    float rz = 0.f, bb = 0.f;
-    for (int32_t f = tid; f < nslots; f += kPipeThreads) {
-      const int32_t i = own_row(f);
-      if (i >= n) continue;
-      const float3 bv = make_float3(a.b[3 * int64_t(i)], a.b[3 * int64_t(i) + 1],
-                                    a.b[3 * int64_t(i) + 2]);
-      const float3 zv = apply_p(ld_sym(a.pinv, a.vs, i), bv);
-      st3(a.r, a.vs, i, bv);
-      st3(a.z, a.vs, i, zv);
-      a.p[i] = make_float4(zv.x, zv.y, zv.z, 0.f);
-      st3(a.dv, a.vs, i, make_float3(0.f, 0.f, 0.f));
-      rz += dot3(bv, zv);
-      bb += dot3(bv, bv);
+  bool run;
+  if constexpr (kGuess) {
+    run = start_from_guess<BW>(a, m, sh, C, L, n, nslots, my_rec, red_sh, &ok_sh, &fail_sh,
+                               &stop_sh, &zero_sh);
+  } else {
+    // ---- init: r = b, z = P b, dv = 0, p = z; partials r.z and b.b ---------
+    {
+      float rz = 0.f, bb = 0.f;
+      for (int32_t f = tid; f < nslots; f += kPipeThreads) {
+        const int32_t i = own_row(f);
+        if (i >= n) continue;
+        const float3 bv = make_float3(a.b[3 * int64_t(i)], a.b[3 * int64_t(i) + 1],
+                                      a.b[3 * int64_t(i) + 2]);
+        const float3 zv = apply_p(ld_sym(a.pinv, a.vs, i), bv);
+        st3(a.r, a.vs, i, bv);
+        st3(a.z, a.vs, i, zv);
+        a.p[i] = make_float4(zv.x, zv.y, zv.z, 0.f);
+        st3(a.dv, a.vs, i, make_float3(0.f, 0.f, 0.f));
+        rz += dot3(bv, zv);
+        bb += dot3(bv, bv);
+      }
+      Dfloat v[2] = {df_of(rz), df_of(bb)};
+      block_sum_df0<kPipeThreads, 2>(v, red_sh);
+      if (tid == 0) {
+        my_rec[REC_RZ] = df_pack(v[0]);
+        my_rec[REC_BB] = df_pack(v[1]);
+      }
     }
-    Dfloat v[2] = {df_of(rz), df_of(bb)};
-    block_sum_df0<kPipeThreads, 2>(v, red_sh);
-    if (tid == 0) {
-      my_rec[REC_RZ] = df_pack(v[0]);
-      my_rec[REC_BB] = df_pack(v[1]);
-    }
-  }
-  bool run = grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh);
+    run = grid_barrier(a.bar, L.epoch, &fail_sh, &ok_sh);
 
-  if (run) {
-    Dfloat v[2], rz[1], bb[1];
-    records_share<1>(a.rec, gridDim.x, REC_RZ, kPipeThreads, rz);
-    records_share<1>(a.rec, gridDim.x, REC_BB, kPipeThreads, bb);
-    v[0] = rz[0];
-    v[1] = bb[0];
-    block_sum_df0<kPipeThreads, 2>(v, red_sh);
-    if (tid == 0) {
-      const double bbd = df_value(v[1]);
-      L.rz_old = df_value(v[0]);
-      L.bbd = bbd;
-      L.rr_last = bbd;
-      int stop = 1;
-      PcgState st{1, 0, PCLOTH_OK, 0, 0.0, sqrt(bbd)};
-      if (!isfinite(bbd)) {
-        st.code = PCLOTH_ERR_NONFINITE;
-        if (blockIdx.x == 0) atomicOr(a.status, ST_NONFINITE);
-      } else if (!(bbd > 0.0)) {
-        st.code = PCLOTH_OK;             // b = 0: dv = 0 is exact
-      } else if (a.maxit <= 0) {
-        st.relres = 1.0;
-        st.code = (1.0 <= a.tol2) ? PCLOTH_OK : PCLOTH_NOT_CONVERGED;
-      } else {
-        stop = 0;
+    if (run) {
+      Dfloat v[2], rz[1], bb[1];
+      records_share<1>(a.rec, gridDim.x, REC_RZ, kPipeThreads, rz);
+      records_share<1>(a.rec, gridDim.x, REC_BB, kPipeThreads, bb);
+      v[0] = rz[0];
+      v[1] = bb[0];
+      block_sum_df0<kPipeThreads, 2>(v, red_sh);
+      if (tid == 0) {
+        const double bbd = df_value(v[1]);
+        L.rz_old = df_value(v[0]);
+        L.bbd = bbd;
+        L.rr_last = bbd;
+        int stop = 1;
+        PcgState st{1, 0, PCLOTH_OK, 0, 0.0, sqrt(bbd)};
+        if (!isfinite(bbd)) {
+          st.code = PCLOTH_ERR_NONFINITE;
+          if (blockIdx.x == 0) atomicOr(a.status, ST_NONFINITE);
+        } else if (!(bbd > 0.0)) {
+          st.code = PCLOTH_OK;             // b = 0: dv = 0 is exact
+        } else if (a.maxit <= 0) {
+          st.relres = 1.0;
+          st.code = (1.0 <= a.tol2) ? PCLOTH_OK : PCLOTH_NOT_CONVERGED;
+        } else {
+          stop = 0;
+        }
+        if (stop && blockIdx.x == 0) *a.state = st;
+        stop_sh = stop;
+        // the first stages of the first SpMV
+        if (!stop) {
+          Producer P = L.P;
+          for (int j = 0; j < kPipeStages && !P.ended; ++j)
+            if (producer_step<BW>(P, sh, m) < 0) timed_out(a.status, &fail_sh);
+          L.P = P;
+        }
       }
-      if (stop && blockIdx.x == 0) *a.state = st;
-      stop_sh = stop;
-      // the first stages of the first SpMV
-      if (!stop) {
-        Producer P = L.P;
-        for (int j = 0; j < kPipeStages && !P.ended; ++j)
-          if (producer_step<BW>(P, sh, m) < 0) timed_out(a.status, &fail_sh);
-        L.P = P;
-      }
+      __syncthreads();
+      run = stop_sh == 0;
     }
-    __syncthreads();
-    run = stop_sh == 0;
   }
 
   if (timer) L.t_prev = now_ns();
@@ -568,10 +702,11 @@ pcg_loop(LoopArgs a) {
       a.phase_ns[3] = L.n_timed;
     }
   }
+  const bool zero = zero_sh != 0;
   for (int32_t f = tid; f < nslots; f += kPipeThreads) {
     const int32_t i = own_row(f);
     if (i >= n) continue;
-    const float3 d = ld3(a.dv, a.vs, i);
+    const float3 d = zero ? make_float3(0.f, 0.f, 0.f) : ld3(a.dv, a.vs, i);
     a.dv_out[3 * int64_t(i)] = d.x;
     a.dv_out[3 * int64_t(i) + 1] = d.y;
     a.dv_out[3 * int64_t(i) + 2] = d.z;
@@ -593,19 +728,19 @@ state_update(int64_t m, float* __restrict__ x, float* __restrict__ v,
   if (!ok) atomicOr(status, ST_NONFINITE);
 }
 
-bool g_loop_attr[2][64] = {};
+bool g_loop_attr[3][64] = {};
 
-template <int BW>
+template <int BW, bool G>
 int loop_attrs(int device) {
-  const int w = BW == kSymBlock ? 0 : 1;
+  const int w = BW == kSymBlock ? (G ? 1 : 0) : 2;
   if (device >= 0 && device < 64 && g_loop_attr[w][device]) return 0;
   constexpr size_t smem = Pipe<BW>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(pcg_loop<BW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(smem));
+  cudaError_t e = cudaFuncSetAttribute(pcg_loop<BW, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   cudaFuncAttributes fa{};
-  if (PCLOTH_PIPE_CARVE && e == cudaSuccess) e = cudaFuncGetAttributes(&fa, pcg_loop<BW>);
+  if (PCLOTH_PIPE_CARVE && e == cudaSuccess) e = cudaFuncGetAttributes(&fa, pcg_loop<BW, G>);
   if (PCLOTH_PIPE_CARVE && e == cudaSuccess)
-    e = cudaFuncSetAttribute(pcg_loop<BW>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(pcg_loop<BW, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              pipe_carveout_percent(smem, fa.sharedSizeBytes));
   if (e != cudaSuccess) return int(e);
   if (device >= 0 && device < 64) g_loop_attr[w][device] = true;
@@ -614,13 +749,13 @@ int loop_attrs(int device) {
 
 // Grid of the persistent kernel: the streaming grid, capped at the CTAs
 // that can be resident at once.
-template <int BW>
+template <int BW, bool G>
 int loop_grid_for(int32_t n, int device, int sm_count, int* grid) {
-  const int e = loop_attrs<BW>(device);
+  const int e = loop_attrs<BW, G>(device);
   if (e != 0) return e;
   int per_sm = 0;
   const cudaError_t o = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, pcg_loop<BW>, kPipeThreads, Pipe<BW>::kSmem);
+      &per_sm, pcg_loop<BW, G>, kPipeThreads, Pipe<BW>::kSmem);
   if (o != cudaSuccess) return int(o);
   if (per_sm <= 0) return int(cudaErrorCooperativeLaunchTooLarge);
   *grid = std::min(spmv_grid_for(n, sm_count), per_sm * sm_count);
@@ -632,13 +767,13 @@ int loop_grid_for(int32_t n, int device, int sm_count, int* grid) {
 // the launch disagree), the grid is halved until it fits -- any grid is
 // correct, each CTA then walks more tiles -- and *grid keeps the size that
 // launched.
-template <int BW>
+template <int BW, bool G>
 cudaError_t launch_loop(const LoopArgs& a, int* grid, cudaStream_t stream) {
   LoopArgs args = a;
   void* params[] = {&args};
   while (true) {
     const cudaError_t e = cudaLaunchCooperativeKernel(
-        reinterpret_cast<const void*>(pcg_loop<BW>), dim3(*grid), dim3(kPipeThreads), params,
+        reinterpret_cast<const void*>(pcg_loop<BW, G>), dim3(*grid), dim3(kPipeThreads), params,
         Pipe<BW>::kSmem, stream);
     if (e != cudaErrorCooperativeLaunchTooLarge || *grid <= 1) return e;
     cudaGetLastError();   // a launch-configuration error: not sticky
@@ -717,9 +852,10 @@ int selftest_bounded_wait(int which, double limit_s, uint32_t* status_out) {
   return PCLOTH_OK;
 }
 
-int pcg_loop_grid(int blk, int32_t n, int device, int sm_count, int* grid) {
-  return blk == kSymBlock ? loop_grid_for<kSymBlock>(n, device, sm_count, grid)
-                          : loop_grid_for<9>(n, device, sm_count, grid);
+int pcg_loop_grid(int blk, int32_t n, int device, int sm_count, int* grid, bool guess) {
+  if (blk != kSymBlock) return loop_grid_for<9, false>(n, device, sm_count, grid);
+  return guess ? loop_grid_for<kSymBlock, true>(n, device, sm_count, grid)
+               : loop_grid_for<kSymBlock, false>(n, device, sm_count, grid);
 }
 
 int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt) {
@@ -730,9 +866,9 @@ int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt
 }
 
 int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iterations,
-              double* rel_residual) {
+              double* rel_residual, const float* x0, bool async) {
   cudaStream_t s = h->stream;
-  const bool prof = h->prof.on;
+  const bool prof = h->prof.on && !async;
   LoopArgs a{};
   a.m = PipeMatrix{h->n, (h->n + kPipeRows - 1) / kPipeRows, h->rowptr, h->colind, h->vals,
                    nullptr, 0};
@@ -749,16 +885,27 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
   a.state = h->state;
   a.status = h->d_status;
   a.dv_out = dv_out;
+  a.x0 = x0;
   a.phase_ns = prof ? h->phase_ns : nullptr;
   a.tol2 = tol * tol;
   a.maxit = maxit;
   cudaError_t e = cudaMemsetAsync(h->bar, 0, sizeof(unsigned long long), s);
   if (e != cudaSuccess) return cuda_fail(h, e, "pcg barrier reset");
   if (prof) cudaEventRecord(h->ev[2], s);
-  e = h->blk == kSymBlock ? launch_loop<kSymBlock>(a, &h->loop_grid, s)
-                          : launch_loop<9>(a, &h->loop_grid, s);
+  if (x0) {
+    if (h->loop_grid_guess <= 0) {
+      const int ge = pcg_loop_grid(kSymBlock, h->n, h->device, h->sm_count, &h->loop_grid_guess,
+                                   true);
+      if (ge != 0) return cuda_fail(h, cudaError_t(ge), "PCG kernel occupancy (guess)");
+    }
+    e = launch_loop<kSymBlock, true>(a, &h->loop_grid_guess, s);
+  } else {
+    e = launch_loop<kSymBlock, false>(a, &h->loop_grid, s);
+  }
   if (e != cudaSuccess) return cuda_fail(h, e, "pcg launch");
   h->launches += 1;
+  // the asynchronous form reads nothing back: pcloth_step_result does, later
+  if (async) return PCLOTH_OK;
   if (prof) cudaEventRecord(h->ev[3], s);
   e = cudaMemcpyAsync(h->state_host, h->state, sizeof(PcgState), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess && prof)
@@ -767,8 +914,6 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
   if (e != cudaSuccess) return cuda_fail(h, e, "pcg state copy");
   int rc = collect_status(h);  // synchronises
   const PcgState st = *h->state_host;
-  if (iterations) *iterations = st.iterations;
-  if (rel_residual) *rel_residual = st.relres;
   if (prof) {
     float ms = 0.f;
     cudaEventElapsedTime(&ms, h->ev[2], h->ev[3]);
@@ -781,6 +926,15 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
     h->prof.spmv_launches += st.iterations;
     h->prof.update_launches += st.iterations;
   }
+  return solve_code(h, rc, st, iterations, rel_residual);
+}
+
+// The outcome of the last solve from its device state, after the status word
+// was collected (rc).
+int solve_code(Handle* h, int rc, const PcgState& st, int32_t* iterations,
+               double* rel_residual) {
+  if (iterations) *iterations = st.iterations;
+  if (rel_residual) *rel_residual = st.relres;
   if (rc != PCLOTH_OK && rc != PCLOTH_ERR_BREAKDOWN && rc != PCLOTH_ERR_NONFINITE) return rc;
   if (st.code != PCLOTH_OK && st.code != PCLOTH_NOT_CONVERGED) {
     fail(h, st.code, st.code == PCLOTH_ERR_BREAKDOWN ? "PCG breakdown (p.Ap <= 0 or r.z <= 0)"
@@ -790,6 +944,14 @@ int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv_out, int32_t* iter
   if (rc != PCLOTH_OK) return rc;
   if (st.code == PCLOTH_NOT_CONVERGED) fail(h, st.code, "PCG reached maxit");
   return st.code;
+}
+
+int pcg_result(Handle* h, int32_t* iterations, double* rel_residual) {
+  cudaError_t e = cudaMemcpyAsync(h->state_host, h->state, sizeof(PcgState),
+                                  cudaMemcpyDeviceToHost, h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "pcg state copy");
+  const int rc = collect_status(h);  // synchronises
+  return solve_code(h, rc, *h->state_host, iterations, rel_residual);
 }
 
 // ===========================================================================
@@ -932,7 +1094,7 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
   cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, device);
   if (sm_count <= 0) sm_count = 1;
   int grid = 0;
-  const int ge = pcg_loop_grid(9, n, device, sm_count, &grid);
+  const int ge = pcg_loop_grid(9, n, device, sm_count, &grid, false);
   if (ge != 0) return cuda_fail(nullptr, cudaError_t(ge), "pcg grid");
   if (grid > kStaticMaxRecords)
     return fail(nullptr, PCLOTH_ERR_CAPACITY, "too many CTAs for the fixed partial sums");
@@ -979,7 +1141,7 @@ int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, co
   bsr3_diag_inverse<<<(n + 255) / 256, 256, 0, stream>>>(n, rowptr, colind, vals, pinv6,
                                                         kStaticPlane, status);
   e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_loop<9>(a, &grid, stream);
+  if (e == cudaSuccess) e = launch_loop<9, false>(a, &grid, stream);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "static solve launch");
   PcgState st{};
   e = cudaMemcpyAsync(&st, a.state, sizeof(PcgState), cudaMemcpyDeviceToHost, stream);

@@ -99,6 +99,7 @@ struct Handle {
   int sm_count = 0;
   int spmv_grid = 0, vec_grid = 0;
   int loop_grid = 0;         // CTAs of the persistent PCG kernel (co-resident)
+  int loop_grid_guess = 0;   // the same for its warm-start form (set on first use)
   int64_t launches = 0;      // kernels launched by this handle
   std::string err;
 
@@ -223,11 +224,20 @@ int launch_vals_expand(Handle* h, float* out9, int64_t nnzb);
 // pcg.cu
 // CTAs of the persistent PCG kernel for blocks of blk floats: the streaming
 // grid, capped at what can be co-resident (a cooperative launch needs all).
-int pcg_loop_grid(int blk, int32_t n, int device, int sm_count, int* grid);
+int pcg_loop_grid(int blk, int32_t n, int device, int sm_count, int* grid, bool guess = false);
 int selftest_bounded_wait(int which, double limit_s, uint32_t* status_out);
+// x0: the initial iterate (device float[n][3], may alias dv), or null for
+// dv = 0.  async: enqueue only -- no host synchronisation or read; the
+// result stays in h->state and the status word (pcloth_step_result).
 int pcg_solve(Handle* h, double tol, int32_t maxit, float* dv,
-              int32_t* iterations, double* rel_residual);
+              int32_t* iterations, double* rel_residual, const float* x0 = nullptr,
+              bool async = false);
 int launch_state_update(Handle* h, float* x, float* v, const float* dv, float dt);
+// The outcome of the last (asynchronous) solve: synchronises, reads its
+// device state and the status word.
+int pcg_result(Handle* h, int32_t* iterations, double* rel_residual);
+int solve_code(Handle* h, int rc, const PcgState& st, int32_t* iterations,
+               double* rel_residual);
 int pcg_solve_static(int32_t n, const int32_t* rowptr, const int32_t* colind, const float* vals,
                      const float* b, double tol, int32_t maxit, float* dv_out,
                      int32_t* iterations, double* rel_residual, cudaStream_t stream);

@@ -31,7 +31,8 @@ EXPORTS = ("pcloth_create", "pcloth_assemble", "pcloth_spmv", "pcloth_solve", "p
            "pcloth_step_host", "pcloth_nnzb", "pcloth_export", "pcloth_set_stream",
            "pcloth_sync", "pcloth_last_error", "pcloth_destroy", "pcloth_profile_enable",
            "pcloth_profile_read", "pcloth_solve_bsr3_static", "pcloth_bell_build",
-           "pcloth_spmv_bell", "pcloth_find_contacts", "pcloth_selftest_bounded_wait")
+           "pcloth_spmv_bell", "pcloth_find_contacts", "pcloth_selftest_bounded_wait",
+           "pcloth_solve_guess", "pcloth_step_async", "pcloth_step_result")
 
 STATIC_MAX_VERTS = 16384   # PCLOTH_STATIC_MAX_VERTS
 
@@ -84,6 +85,9 @@ def lib():
                                   P(i32), P(dbl)]
         L.pcloth_step_host.argtypes = [vp, vp, vp, P(Springs), ctypes.c_float, dbl, i32,
                                        P(i32), P(dbl)]
+        L.pcloth_solve_guess.argtypes = [vp, dbl, i32, vp, P(i32), P(dbl)]
+        L.pcloth_step_async.argtypes = [vp, vp, vp, P(Springs), ctypes.c_float, dbl, i32, vp]
+        L.pcloth_step_result.argtypes = [vp, P(i32), P(dbl)]
         L.pcloth_nnzb.argtypes = [vp, P(i64)]
         L.pcloth_export.argtypes = [vp, vp, vp, vp, vp, vp]
         L.pcloth_set_stream.argtypes = [vp, vp]
@@ -235,6 +239,42 @@ def pcloth_solve(h: int, tol: float, maxit: int, dv: torch.Tensor):
     rr = ctypes.c_double(0.0)
     rc = lib().pcloth_solve(h, float(tol), int(maxit), _ptr(dv), ctypes.byref(it),
                             ctypes.byref(rr))
+    if rc not in (OK, NOT_CONVERGED):
+        _raise(h, rc)
+    return int(it.value), float(rr.value), rc
+
+
+def pcloth_solve_guess(h: int, tol: float, maxit: int, dv: torch.Tensor):
+    """PCG from the guess held in dv (overwritten with the solution).
+    Returns (iterations, rel_residual, code) like pcloth_solve."""
+    _check(dv, torch.float32, None, None, "dv")
+    it = ctypes.c_int32(0)
+    rr = ctypes.c_double(0.0)
+    rc = lib().pcloth_solve_guess(h, float(tol), int(maxit), _ptr(dv), ctypes.byref(it),
+                                  ctypes.byref(rr))
+    if rc not in (OK, NOT_CONVERGED):
+        _raise(h, rc)
+    return int(it.value), float(rr.value), rc
+
+
+def pcloth_step_async(h: int, x: torch.Tensor, v: torch.Tensor, contacts, dt: float,
+                      tol: float, maxit: int, dv: Optional[torch.Tensor] = None):
+    """Enqueue one whole step (no host synchronisation); contacts: device
+    (i, j, k, rest) tensors kept alive by the caller, or None."""
+    _check(x, torch.float32, None, None, "x")
+    _check(v, torch.float32, x.device, tuple(x.shape), "v")
+    c = _elements(contacts, x.device, "contacts")
+    rc = lib().pcloth_step_async(h, _ptr(x), _ptr(v), ctypes.byref(c), float(dt), float(tol),
+                                 int(maxit), _ptr(dv))
+    if rc != OK:
+        _raise(h, rc)
+
+
+def pcloth_step_result(h: int):
+    """(iterations, rel_residual, code) of the last asynchronous step."""
+    it = ctypes.c_int32(0)
+    rr = ctypes.c_double(0.0)
+    rc = lib().pcloth_step_result(h, ctypes.byref(it), ctypes.byref(rr))
     if rc not in (OK, NOT_CONVERGED):
         _raise(h, rc)
     return int(it.value), float(rr.value), rc
@@ -446,6 +486,26 @@ class PCloth:
         _check(dv, torch.float32, self.device, (self.n, 3), "dv")
         it, rr, code = pcloth_solve(self.h, tol, maxit, dv)
         return dv, it, rr, code
+
+    def solve_guess(self, dv: torch.Tensor, tol: float, maxit: int):
+        """PCG from the guess in dv (device float32 [n, 3], overwritten)."""
+        _check(dv, torch.float32, self.device, (self.n, 3), "dv")
+        it, rr, code = pcloth_solve_guess(self.h, tol, maxit, dv)
+        return dv, it, rr, code
+
+    def set_stream(self, stream: int):
+        pcloth_set_stream(self.h, stream)
+
+    def step_async(self, x, v, contacts=None, dt: float = 1e-2, tol: float = 1e-6,
+                   maxit: int = 20000, dv: Optional[torch.Tensor] = None):
+        """Enqueue one step without synchronising (capturable in a CUDA graph);
+        contacts: device (i, j, k, rest) tensors that the caller keeps alive
+        (a captured graph reads the same arrays at every replay), or None."""
+        _check(x, torch.float32, self.device, (self.n, 3), "x")
+        pcloth_step_async(self.h, x, v, contacts, dt, tol, maxit, dv)
+
+    def step_result(self):
+        return pcloth_step_result(self.h)
 
     def step(self, x, v, contacts=None, dt: float = 1e-2, tol: float = 1e-6,
              maxit: int = 20000, dv: Optional[torch.Tensor] = None):
