@@ -245,10 +245,23 @@ __device__ __forceinline__ float excess_sq(float3 hi, float3 lo, float L0) {
   return s + small;
 }
 
+// The same for an edge held in one fp32 vector (no lo part).
+__device__ __forceinline__ float excess_sq(float3 v, float L0) {
+  const float px = v.x * v.x, py = v.y * v.y, pz = v.z * v.z, pl = -(L0 * L0);
+  const float rx = fmaf(v.x, v.x, -px), ry = fmaf(v.y, v.y, -py);
+  const float rz = fmaf(v.z, v.z, -pz), rl = fmaf(-L0, L0, -pl);
+  float s, t1, t2, t3;
+  two_sum(px, py, s, t1);
+  two_sum(s, pz, s, t2);
+  two_sum(s, pl, s, t3);
+  return s + (((t1 + t2) + t3) + (((rx + ry) + rz) + rl));
+}
+
 // Scaled stiffness block K' = -h^2 K (6 unique entries of the symmetric
 // block) and force F of one element seen from vertex i: K at x, force at
-// x~ = x + h v.  e = x_j - x_i (exact, see Edge) is shared by all elements of
-// a block and w = v_j - v_i.
+// x~ = x + h v.  e = x_j - x_i (exact, see Edge), its length and the
+// advanced edge are shared by all elements of a block (BlockEdge, formed
+// once per block); each element costs two divisions.
 //
 // K = a I + c d d^T with a = k max(0, 1 - L0/l), c = k - a.  The length
 // excess l - L0 is formed as (|e|^2 - L0^2) / (l + L0) with the squares in
@@ -271,34 +284,52 @@ __device__ __forceinline__ float scaled_entry(float S, float hr, float lr, float
   return fmaf(S, p, S * tail);
 }
 
-__device__ __forceinline__ void element_terms(const Edge& e, float3 w, float dt, float h2,
-                                              float k, float L0, float (&K)[6], float (&F)[3]) {
-  const float3 h = e.hi, o = e.lo;
-  const float l2 = fmaf(h.x, h.x, fmaf(h.y, h.y, h.z * h.z)) +
-                   2.0f * fmaf(h.x, o.x, fmaf(h.y, o.y, h.z * o.z));
-  const float l = sqrtf(l2);
-  const float stretch = excess_sq(h, o, L0) / (l + L0);    // l - L0
-  const float tension = fmaxf(0.0f, stretch / l);                  // max(0, 1 - L0/l)
+// What the elements of one block share: the edge at x_t (exact, with
+// l2 = |e|^2, l = |e| and 1 / l2) and the advanced edge at x~ with its length.
+struct BlockEdge {
+  Edge e;
+  float l2, l, inv_l2;
+  float3 adv;
+  float lt;
+};
+
+__device__ __forceinline__ BlockEdge block_edge(float3 xi, float3 xj, float3 vi, float3 vj,
+                                                float dt) {
+  BlockEdge b;
+  b.e = edge_of(xi, xj);
+  const float3 h = b.e.hi, o = b.e.lo;
+  b.l2 = fmaf(h.x, h.x, fmaf(h.y, h.y, h.z * h.z)) +
+         2.0f * fmaf(h.x, o.x, fmaf(h.y, o.y, h.z * o.z));
+  b.l = sqrtf(b.l2);
+  b.inv_l2 = 1.0f / b.l2;
+  const float3 w = make_float3(vj.x - vi.x, vj.y - vi.y, vj.z - vi.z);
+  b.adv = make_float3(fmaf(dt, w.x, h.x) + o.x, fmaf(dt, w.y, h.y) + o.y,
+                      fmaf(dt, w.z, h.z) + o.z);
+  b.lt = sqrtf(b.adv.x * b.adv.x + b.adv.y * b.adv.y + b.adv.z * b.adv.z);
+  return b;
+}
+
+__device__ __forceinline__ void element_terms(const BlockEdge& b, float h2, float k, float L0,
+                                              float (&K)[6], float (&F)[3]) {
+  const float3 h = b.e.hi, o = b.e.lo;
+  const float l = b.l;
+  // max(0, 1 - L0/l) = max(0, (l - L0) / l), with l - L0 = (|e|^2 - L0^2) / (l + L0)
+  const float tension = fmaxf(0.0f, excess_sq(h, o, L0) / ((l + L0) * l));
   const float a = k * tension;
   const float c = k - a;
   const float A = -h2 * a;
-  const float S = (-h2 * c) / l2;
+  const float S = (-h2 * c) * b.inv_l2;
   K[0] += scaled_entry(S, h.x, o.x, h.x, o.x) + A;
   K[1] += scaled_entry(S, h.x, o.x, h.y, o.y);
   K[2] += scaled_entry(S, h.x, o.x, h.z, o.z);
   K[3] += scaled_entry(S, h.y, o.y, h.y, o.y) + A;
   K[4] += scaled_entry(S, h.y, o.y, h.z, o.z);
   K[5] += scaled_entry(S, h.z, o.z, h.z, o.z) + A;
-  // force at the advanced positions
-  const float fx = fmaf(dt, w.x, h.x) + o.x, fy = fmaf(dt, w.y, h.y) + o.y,
-              fz = fmaf(dt, w.z, h.z) + o.z;
-  const float lt = sqrtf(fx * fx + fy * fy + fz * fz);
-  const float3 fz3 = make_float3(0.f, 0.f, 0.f);
-  const float st = excess_sq(make_float3(fx, fy, fz), fz3, L0) / (lt + L0);   // l~ - L0
-  const float s = k * st / lt;
-  F[0] += s * fx;
-  F[1] += s * fy;
-  F[2] += s * fz;
+  // force at the advanced positions: k (l~ - L0) / l~ along the advanced edge
+  const float s = k * excess_sq(b.adv, L0) / ((b.lt + L0) * b.lt);
+  F[0] += s * b.adv.x;
+  F[1] += s * b.adv.y;
+  F[2] += s * b.adv.z;
 }
 
 __device__ __forceinline__ float3 ld3(const float* p, int64_t i) {
@@ -440,13 +471,12 @@ assemble_rows(AsmArgs a) {
     }
     float K[6] = {0, 0, 0, 0, 0, 0}, F[3] = {0, 0, 0};
     const float3 xj = ld3(a.x, col), vj = ld3(a.v, col);
-    const Edge ed = edge_of(xi, xj);
-    const float3 wd = make_float3(vj.x - vi.x, vj.y - vi.y, vj.z - vi.z);
+    const BlockEdge be = block_edge(xi, xj, vi, vj, a.dt);
     if (sslot >= 0) {
       const int32_t e1 = a.sblk_ptr[sslot + 1];
       for (int32_t e = a.sblk_ptr[sslot]; e < e1; ++e) {
         const float2 kl = a.sentry[e];
-        element_terms(ed, wd, a.dt, a.h2, kl.x, kl.y, K, F);
+        element_terms(be, a.h2, kl.x, kl.y, K, F);
       }
     }
     // the block's contacts: a run of entries with this column
@@ -459,7 +489,7 @@ assemble_rows(AsmArgs a) {
       const uint64_t en = a.centry[t];
       if (int32_t(en >> 32) != col) break;
       const int32_t c = int32_t(uint32_t(en));
-      element_terms(ed, wd, a.dt, a.h2, a.ck[c], a.cr[c], K, F);
+      element_terms(be, a.h2, a.ck[c], a.cr[c], K, F);
     }
     if (live) {
       float* dst = a.vals + kSymBlock * (int64_t(ob) + p);
