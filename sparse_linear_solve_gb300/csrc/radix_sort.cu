@@ -1,13 +1,13 @@
 // Stable LSD radix sort of (uint64 key, int32 value) pairs and an exclusive
-// int32 scan, for the per-step contact keys.
+// int32 scan.
 //
-// P-Cloth (arXiv 2008.00409) Sec. 3.2.2 fills the index table with atomics
-// and then sorts every row and removes duplicates, one thread per row.  Here
-// the contact entries are instead sorted globally by (row, col) key, so rows
-// need no per-thread sort and the order of equal keys (their input order) is
-// deterministic.  Each pass over one 8-bit digit is three kernels: per-tile
-// digit histograms, one exclusive scan of the digit-major histogram table,
-// and a stable scatter that ranks keys inside each warp with match_any.
+// The sort orders the vertices by spatial-hash cell and the found contact
+// pairs by (i, j) for contact finding (contacts.cu; P-Cloth Sec. 4.2): equal
+// keys keep their input order, so the results are deterministic.  Each pass
+// over one 8-bit digit is three kernels: per-tile digit histograms, one
+// exclusive scan of the digit-major histogram table, and a stable scatter
+// that ranks keys inside each warp with match_any.  The scan also serves
+// the assembly's per-row counts (assemble.cu).
 
 #include "pcloth_internal.cuh"
 

@@ -3,7 +3,7 @@
 // pcloth_spmv.  One persistent CTA per (SM x kPipeCtasPerSm) streams its row
 // tiles through the pipeline of spmv_pipe.cuh once; the input and output
 // are the caller's float[n][3] vectors.  The PCG solve runs the same
-// pipeline inside its persistent kernel (pcg_loop.cu).
+// pipeline inside its persistent kernel (pcg.cu).
 
 #include <algorithm>
 

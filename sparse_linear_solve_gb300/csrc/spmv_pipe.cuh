@@ -1,6 +1,6 @@
 // Streaming pipeline of the block (3x3) sparse matrix-vector product: the
 // machinery shared by the plain product q = A x (spmv.cu) and the SpMV phase
-// of the persistent PCG kernel (pcg_loop.cu).  P-Cloth (arXiv 2008.00409,
+// of the persistent PCG kernel (pcg.cu).  P-Cloth (arXiv 2008.00409,
 // Sec. 3.1): SpMV is the most expensive operator of the PCG solve; Eq. (4)
 // with one GPU is the plain product.
 //
