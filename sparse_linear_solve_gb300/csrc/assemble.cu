@@ -16,7 +16,7 @@
 //                     and lists the columns that are not spring blocks: the
 //                     row's new blocks
 //   scan              new blocks before each row
-//   assemble_rows     16 lanes per row: the row's blocks in column order
+//   assemble_rows     two lanes per row: the row's blocks in column order
 //                     (spring and new blocks merged), every element of every
 //                     off-diagonal block evaluated and written, the row's
 //                     compensated sum into its diagonal block, b = h f and
@@ -224,7 +224,10 @@ __device__ __forceinline__ Edge edge_of(float3 xi, float3 xj) {
 // 2 hi.lo and lo.lo (all about 2^-24 of the squares or smaller) are added in
 // plain fp32.  The error is about 2^-48 |e|^2, like an fp64 evaluation, at
 // fp32 speed (fp64 is a slow path on this GPU).  Every term is even in e, so
-// the edges e and -e give the same bits.
+// the edges e and -e give the same bits.  The squares are rounded with
+// __fmul_rn, which the compiler never fuses into a multiply-add: fused into
+// the TwoSum that follows, a square would enter that sum unrounded and its
+// error term would no longer be exact.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& t) {
   s = a + b;
   const float bp = s - a;
@@ -232,7 +235,8 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& t) {
 }
 
 __device__ __forceinline__ float excess_sq(float3 hi, float3 lo, float L0) {
-  const float px = hi.x * hi.x, py = hi.y * hi.y, pz = hi.z * hi.z, pl = -(L0 * L0);
+  const float px = __fmul_rn(hi.x, hi.x), py = __fmul_rn(hi.y, hi.y);
+  const float pz = __fmul_rn(hi.z, hi.z), pl = -__fmul_rn(L0, L0);
   const float rx = fmaf(hi.x, hi.x, -px), ry = fmaf(hi.y, hi.y, -py);
   const float rz = fmaf(hi.z, hi.z, -pz), rl = fmaf(-L0, L0, -pl);
   float s, t1, t2, t3;
@@ -247,7 +251,8 @@ __device__ __forceinline__ float excess_sq(float3 hi, float3 lo, float L0) {
 
 // The same for an edge held in one fp32 vector (no lo part).
 __device__ __forceinline__ float excess_sq(float3 v, float L0) {
-  const float px = v.x * v.x, py = v.y * v.y, pz = v.z * v.z, pl = -(L0 * L0);
+  const float px = __fmul_rn(v.x, v.x), py = __fmul_rn(v.y, v.y);
+  const float pz = __fmul_rn(v.z, v.z), pl = -__fmul_rn(L0, L0);
   const float rx = fmaf(v.x, v.x, -px), ry = fmaf(v.y, v.y, -py);
   const float rz = fmaf(v.z, v.z, -pz), rl = fmaf(-L0, L0, -pl);
   float s, t1, t2, t3;
@@ -261,7 +266,11 @@ __device__ __forceinline__ float excess_sq(float3 v, float L0) {
 // block) and force F of one element seen from vertex i: K at x, force at
 // x~ = x + h v.  e = x_j - x_i (exact, see Edge), its length and the
 // advanced edge are shared by all elements of a block (BlockEdge, formed
-// once per block); each element costs two divisions.
+// once per block); each element costs two divisions.  Lengths come from
+// rsqrtf and the two quotients from __fdividef, each good to a few units in
+// the last place (~1e-7 relative): far inside the 1e-5 to which every block
+// is checked against the fp64 oracle, and the length excess, whose
+// cancellation is what needs care, is formed exactly beforehand.
 //
 // K = a I + c d d^T with a = k max(0, 1 - L0/l), c = k - a.  The length
 // excess l - L0 is formed as (|e|^2 - L0^2) / (l + L0) with the squares in
@@ -300,12 +309,14 @@ __device__ __forceinline__ BlockEdge block_edge(float3 xi, float3 xj, float3 vi,
   const float3 h = b.e.hi, o = b.e.lo;
   b.l2 = fmaf(h.x, h.x, fmaf(h.y, h.y, h.z * h.z)) +
          2.0f * fmaf(h.x, o.x, fmaf(h.y, o.y, h.z * o.z));
-  b.l = sqrtf(b.l2);
-  b.inv_l2 = 1.0f / b.l2;
+  const float rl = rsqrtf(b.l2);
+  b.l = b.l2 * rl;
+  b.inv_l2 = rl * rl;
   const float3 w = make_float3(vj.x - vi.x, vj.y - vi.y, vj.z - vi.z);
   b.adv = make_float3(fmaf(dt, w.x, h.x) + o.x, fmaf(dt, w.y, h.y) + o.y,
                       fmaf(dt, w.z, h.z) + o.z);
-  b.lt = sqrtf(b.adv.x * b.adv.x + b.adv.y * b.adv.y + b.adv.z * b.adv.z);
+  const float lt2 = b.adv.x * b.adv.x + b.adv.y * b.adv.y + b.adv.z * b.adv.z;
+  b.lt = lt2 * rsqrtf(lt2);
   return b;
 }
 
@@ -314,7 +325,7 @@ __device__ __forceinline__ void element_terms(const BlockEdge& b, float h2, floa
   const float3 h = b.e.hi, o = b.e.lo;
   const float l = b.l;
   // max(0, 1 - L0/l) = max(0, (l - L0) / l), with l - L0 = (|e|^2 - L0^2) / (l + L0)
-  const float tension = fmaxf(0.0f, excess_sq(h, o, L0) / ((l + L0) * l));
+  const float tension = fmaxf(0.0f, __fdividef(excess_sq(h, o, L0), (l + L0) * l));
   const float a = k * tension;
   const float c = k - a;
   const float A = -h2 * a;
@@ -326,7 +337,7 @@ __device__ __forceinline__ void element_terms(const BlockEdge& b, float h2, floa
   K[4] += scaled_entry(S, h.y, o.y, h.z, o.z);
   K[5] += scaled_entry(S, h.z, o.z, h.z, o.z) + A;
   // force at the advanced positions: k (l~ - L0) / l~ along the advanced edge
-  const float s = k * excess_sq(b.adv, L0) / ((b.lt + L0) * b.lt);
+  const float s = k * __fdividef(excess_sq(b.adv, L0), (b.lt + L0) * b.lt);
   F[0] += s * b.adv.x;
   F[1] += s * b.adv.y;
   F[2] += s * b.adv.z;
@@ -336,7 +347,20 @@ __device__ __forceinline__ float3 ld3(const float* p, int64_t i) {
   return make_float3(p[3 * i], p[3 * i + 1], p[3 * i + 2]);
 }
 
-// Merge position p of two sorted disjoint lists S (static cols) and T (new
+// Writes a packed block (six floats from float offset 6 q) with one 16-byte
+// and one 8-byte store, without a branch: 24 q bytes is 16-byte aligned for
+// even q, so the 16-byte word holds entries 0-3 there and 2-5 for odd q.
+// Six 4-byte stores from the lanes of a warp, whose blocks lie in 16
+// different rows, reach L2 as six partial-sector writes per block.
+__device__ __forceinline__ void st_block(float* vals, int64_t q, const float (&K)[6]) {
+  float* d = vals + kSymBlock * q;
+  const bool odd = (q & 1) != 0;
+  const float4 w4 =
+      odd ? make_float4(K[2], K[3], K[4], K[5]) : make_float4(K[0], K[1], K[2], K[3]);
+  const float2 w2 = odd ? make_float2(K[0], K[1]) : make_float2(K[4], K[5]);
+  *reinterpret_cast<float4*>(d + (odd ? 2 : 0)) = w4;
+  *reinterpret_cast<float2*>(d + (odd ? 0 : 4)) = w2;
+}
 
 // Merge position p of two sorted disjoint column lists S (spring blocks) and
 // T (new blocks): returns the number of S entries before position p.
@@ -390,27 +414,26 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, int64_t 
   a.pinv6[3 * a.vs + i] = c11 * id;
   a.pinv6[4 * a.vs + i] = c12 * id;
   a.pinv6[5 * a.vs + i] = c22 * id;
-#pragma unroll
-  for (int t = 0; t < kSymBlock; ++t) a.vals[kSymBlock * dpos + t] = D[t];
+  st_block(a.vals, dpos, D);
   bool ok = finite3(b0, b1, b2) && isfinite(det) && det > 0.0f;
 #pragma unroll
   for (int t = 0; t < kSymBlock; ++t) ok = ok && isfinite(D[t]);
   if (!ok) atomicOr(a.status, ST_NONFINITE);
 }
 
-// Four CTAs per SM (64 registers a thread): the kernel is bound by the
-// latency of its gathers and of the per-row reductions, so occupancy pays
-
-// kRowLanes lanes per row.  Lane l takes the row's blocks l, l + kRowLanes,
-// ... in column order: it finds the block's column (the spring pattern and
-// the row's new blocks merged), evaluates every element of the block -- the
-// spring entries of a spring block, then the block's contacts in input
-// order -- writes the block's column and, off the diagonal, its packed
-// value, and adds the negated value and the block's force into its
+// kRowLanes lanes per row.  The diagonal's position dpos in the row is
+// found first (the spring columns below i plus the new columns below i);
+// lane l then takes the row's off-diagonal blocks l, l + kRowLanes, ... in
+// column order (block k sits at slot k + (k >= dpos)): it finds the block's
+// column (the spring pattern and the row's new blocks merged), evaluates
+// every element of the block -- the spring entries of a spring block, then
+// the block's contacts in input order -- writes the block's column and
+// packed value, and adds the negated value and the block's force into its
 // compensated (TwoSum) partial sums.  A butterfly whose steps are
 // commutative merges the lanes' partials (all lanes end with the same
-// bits), and lane 0 forms the diagonal block, b and the block-Jacobi
-// inverse.  Rows are independent: no shared memory and no CTA barrier.
+// bits), and lane 0 writes the diagonal's column and forms the diagonal
+// block, b and the block-Jacobi inverse.  Rows are independent: no shared
+// memory and no CTA barrier.
 //
 // Two lanes per row at three CTAs per SM (80 registers) were the fastest of
 // a sweep on the 1.65M-triangle cloth (whole assembly per step): 16 lanes
@@ -418,6 +441,10 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, int64_t 
 // 0.47 ms, 1 lane 0.62 ms; four or more CTAs per SM spill and lose.  Fewer
 // lanes cut the butterfly's and the row finish's share of the
 // instructions; one lane per row leaves each row's loads in a serial chain.
+// On that cloth the kernel then took 380 us (ncu); rsqrtf and __fdividef for
+// the IEEE square roots and divisions, the block stores as one 16- and one
+// 8-byte word, and the diagonal taken out of the lanes' loop brought it to
+// 276 us (the whole assembly 0.45 -> 0.345 ms per step).
 #ifndef PCLOTH_ASM_CTAS
 #define PCLOTH_ASM_CTAS 3
 #endif
@@ -445,8 +472,18 @@ assemble_rows(AsmArgs a) {
   }
   const float3 xi = ld3(a.x, i), vi = ld3(a.v, i);
   float Ks[6] = {0, 0, 0, 0, 0, 0}, Kc[6] = {0, 0, 0, 0, 0, 0}, Fs[3] = {0, 0, 0};
-  int32_t dpos = -1;   // position of the diagonal block in the row
-  for (int32_t p = lane; p < len; p += kRowLanes) {
+  int32_t dpos;   // the diagonal's position in the row
+  {
+    int32_t lo = sb, hi = se;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi) >> 1;
+      if (a.colind_s[mid] < i) lo = mid + 1; else hi = mid;
+    }
+    dpos = lo - sb;
+    for (int32_t t = 0; t < nT; ++t) dpos += a.newcol[eb + t] < i;
+  }
+  for (int32_t k = lane; k < len - 1; k += kRowLanes) {
+    const int32_t p = k + (k >= dpos);
     int32_t col, sslot = -1, nk = -1;
     if (nT == 0) {
       sslot = sb + p;
@@ -465,10 +502,6 @@ assemble_rows(AsmArgs a) {
       }
     }
     if (live) a.colind[ob + p] = col;
-    if (col == i) {
-      dpos = p;
-      continue;
-    }
     float K[6] = {0, 0, 0, 0, 0, 0}, F[3] = {0, 0, 0};
     const float3 xj = ld3(a.x, col), vj = ld3(a.v, col);
     const BlockEdge be = block_edge(xi, xj, vi, vj, a.dt);
@@ -492,9 +525,7 @@ assemble_rows(AsmArgs a) {
       element_terms(be, a.h2, a.ck[c], a.cr[c], K, F);
     }
     if (live) {
-      float* dst = a.vals + kSymBlock * (int64_t(ob) + p);
-#pragma unroll
-      for (int t = 0; t < kSymBlock; ++t) dst[t] = K[t];
+      st_block(a.vals, int64_t(ob) + p, K);
     }
     // the diagonal takes -(the block as stored), so that the rows of A sum
     // to M up to the compensated sums' own error
@@ -520,13 +551,10 @@ assemble_rows(AsmArgs a) {
     }
 #pragma unroll
     for (int t = 0; t < 3; ++t) Fs[t] += __shfl_xor_sync(0xffffffffu, Fs[t], off);
-    dpos = max(dpos, __shfl_xor_sync(0xffffffffu, dpos, off));
   }
   if (live && lane == 0) {
-    if (dpos >= 0)
-      finish_row(a, i, int64_t(ob) + dpos, Ks, Kc, Fs);
-    else
-      atomicOr(a.status, ST_CAPACITY);   // diagonal missing: cannot happen
+    a.colind[ob + dpos] = i;
+    finish_row(a, i, int64_t(ob) + dpos, Ks, Kc, Fs);
   }
 }
 
