@@ -36,7 +36,7 @@ void free_handle(Handle* h) {
                   h->rowptr, h->colind, h->vals, h->rhs, h->vec_arena,
                   h->ckey[0], h->ckey[1], h->cval[0], h->cval[1],
                   h->sort_counts, h->scan_tmp, h->rowcnt, h->newcnt, h->newcol,
-                  h->newfirst, h->counters,
+                  h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
                   h->dv, h->rec, h->bar,
                   h->phase_ns, h->state, h->d_status, h->bell_wmax, h->bell_col, h->bell_val,
@@ -269,7 +269,6 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->rowcnt, 2 * (n + 1)));
   A(dalloc(&h->newcnt, n + 1));
   A(dalloc(&h->newcol, ent2));
-  A(dalloc(&h->newfirst, ent2));
   A(dalloc(&h->counters, 4));
   A(dalloc(&h->hx, 3 * n));
   A(dalloc(&h->hv, 3 * n));

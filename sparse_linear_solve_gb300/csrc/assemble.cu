@@ -58,7 +58,6 @@ struct AsmArgs {
   const int32_t* nbefore;   // [n+1] new blocks before each row
   const uint64_t* centry;   // entries, per row sorted by (column << 32 | contact id)
   const int32_t* newcol;    // a row's new columns, at the row's first entry index
-  const int32_t* newfirst;  // the entry index of each new column's first entry
   const float* ck;
   const float* cr;
   int32_t* rowptr;
@@ -157,7 +156,7 @@ __device__ __forceinline__ bool static_has(const int32_t* __restrict__ colind_s,
 __global__ void row_classify(int32_t n, const int32_t* __restrict__ ebefore,
                              uint64_t* __restrict__ centry, const int32_t* __restrict__ rowptr_s,
                              const int32_t* __restrict__ colind_s, int32_t* __restrict__ newcol,
-                             int32_t* __restrict__ newfirst, int32_t* __restrict__ newcnt) {
+                             int32_t* __restrict__ newcnt) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i > n) return;
   if (i == n) {
@@ -176,22 +175,11 @@ __global__ void row_classify(int32_t n, const int32_t* __restrict__ ebefore,
       last = col;
       if (!static_has(colind_s, s0, s1, col)) {
         newcol[e0 + k] = col;
-        newfirst[e0 + k] = t;
         ++k;
       }
     }
   }
   newcnt[i] = k;
-}
-
-__device__ __forceinline__ int32_t lower_bound_col(const uint64_t* __restrict__ a, int32_t lo,
-                                                   int32_t hi, int32_t col) {
-  const uint64_t key = uint64_t(uint32_t(col)) << 32;
-  while (lo < hi) {
-    const int32_t mid = (lo + hi) >> 1;
-    if (a[mid] < key) lo = mid + 1; else hi = mid;
-  }
-  return lo;
 }
 
 // An edge vector carried exactly as hi + lo: the difference of two fp32
@@ -425,11 +413,11 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, int64_t 
 // found first (the spring columns below i plus the new columns below i);
 // lane l then takes the row's off-diagonal blocks l, l + kRowLanes, ... in
 // column order (block k sits at slot k + (k >= dpos)): it finds the block's
-// column (the spring pattern and the row's new blocks merged), evaluates
+// column by walking the spring and new columns with two cursors, evaluates
 // every element of the block -- the spring entries of a spring block, then
-// the block's contacts in input order -- writes the block's column and
-// packed value, and adds the negated value and the block's force into its
-// compensated (TwoSum) partial sums.  A butterfly whose steps are
+// the block's contacts in input order, found by a third cursor -- writes
+// the block's column and packed value, and adds the negated value and the
+// block's force into its compensated (TwoSum) partial sums.  A butterfly whose steps are
 // commutative merges the lanes' partials (all lanes end with the same
 // bits), and lane 0 writes the diagonal's column and forms the diagonal
 // block, b and the block-Jacobi inverse.  Rows are independent: no shared
@@ -444,7 +432,11 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, int64_t 
 // On that cloth the kernel then took 380 us (ncu); rsqrtf and __fdividef for
 // the IEEE square roots and divisions, the block stores as one 16- and one
 // 8-byte word, and the diagonal taken out of the lanes' loop brought it to
-// 276 us (the whole assembly 0.45 -> 0.345 ms per step).
+// 276 us (the whole assembly 0.45 -> 0.345 ms per step).  Contacts cost
+// the most per element: without them the assembly took 0.20 ms.  One
+// element loop for springs and contacts, and cursors in place of a
+// merge-path search per block and a search of the contact run, brought
+// the whole assembly to 0.30 ms.
 #ifndef PCLOTH_ASM_CTAS
 #define PCLOTH_ASM_CTAS 3
 #endif
@@ -482,47 +474,63 @@ assemble_rows(AsmArgs a) {
     dpos = lo - sb;
     for (int32_t t = 0; t < nT; ++t) dpos += a.newcol[eb + t] < i;
   }
+  // Cursors that walk the row with the lane: sc into the spring columns S
+  // and tn into the new columns T (heads hs and ht, kEnd past the end), and
+  // tc into the row's sorted contact entries (head hen).  The lane's first
+  // block is found by a merge-path search, each later one by stepping the
+  // cursors over the other lane's blocks.
+  const int32_t* S = a.colind_s + sb;
+  const int32_t* T = a.newcol + eb;
+  constexpr int32_t kEnd = INT32_MAX;
+  int32_t sc, tn, hs, ht;
+  {
+    const int32_t p0 = lane + (lane >= dpos);
+    sc = merge_split(S, nS, T, nT, p0);
+    tn = p0 - sc;
+    hs = sc < nS ? S[sc] : kEnd;
+    ht = tn < nT ? T[tn] : kEnd;
+  }
+  int32_t tc = eb;
+  uint64_t hen = tc < ee ? a.centry[tc] : ~uint64_t(0);
   for (int32_t k = lane; k < len - 1; k += kRowLanes) {
     const int32_t p = k + (k >= dpos);
-    int32_t col, sslot = -1, nk = -1;
-    if (nT == 0) {
-      sslot = sb + p;
-      col = a.colind_s[sslot];
-    } else {
-      const int32_t* S = a.colind_s + sb;
-      const int32_t* T = a.newcol + eb;
-      const int32_t s = merge_split(S, nS, T, nT, p);
-      const int32_t t = p - s;
-      if (s < nS && (t >= nT || S[s] < T[t])) {
-        sslot = sb + s;
-        col = S[s];
-      } else {
-        nk = t;
-        col = T[t];
-      }
-    }
+    const bool from_s = hs < ht;   // the two lists are disjoint
+    const int32_t col = from_s ? hs : ht;
+    const int32_t sslot = from_s ? sb + sc : -1;
     if (live) a.colind[ob + p] = col;
     float K[6] = {0, 0, 0, 0, 0, 0}, F[3] = {0, 0, 0};
     const float3 xj = ld3(a.x, col), vj = ld3(a.v, col);
     const BlockEdge be = block_edge(xi, xj, vi, vj, a.dt);
+    // The block's elements in one loop, so that the lanes of a warp
+    // evaluate springs and contacts in the same passes: the spring entries,
+    // then the block's contacts, the run of the row's sorted entries with
+    // this column (the contact cursor first passes the entries of the other
+    // lane's columns).
+    int32_t e = 0, e1 = 0;
     if (sslot >= 0) {
-      const int32_t e1 = a.sblk_ptr[sslot + 1];
-      for (int32_t e = a.sblk_ptr[sslot]; e < e1; ++e) {
-        const float2 kl = a.sentry[e];
-        element_terms(be, a.h2, kl.x, kl.y, K, F);
-      }
+      e = a.sblk_ptr[sslot];
+      e1 = a.sblk_ptr[sslot + 1];
     }
-    // the block's contacts: a run of entries with this column
-    int32_t t0 = ee;
-    if (nk >= 0)
-      t0 = a.newfirst[eb + nk];
-    else if (ee > eb)
-      t0 = lower_bound_col(a.centry, eb, ee, col);
-    for (int32_t t = t0; t < ee; ++t) {
-      const uint64_t en = a.centry[t];
-      if (int32_t(en >> 32) != col) break;
-      const int32_t c = int32_t(uint32_t(en));
-      element_terms(be, a.h2, a.ck[c], a.cr[c], K, F);
+    const uint64_t col_key = uint64_t(uint32_t(col)) << 32;
+    while (hen < col_key) {
+      ++tc;
+      hen = tc < ee ? a.centry[tc] : ~uint64_t(0);
+    }
+    while (true) {
+      float kk, L0;
+      if (e < e1) {
+        const float2 kl = a.sentry[e++];
+        kk = kl.x;
+        L0 = kl.y;
+      } else {
+        if ((hen >> 32) != uint64_t(uint32_t(col))) break;
+        const int32_t c = int32_t(uint32_t(hen));
+        kk = a.ck[c];
+        L0 = a.cr[c];
+        ++tc;
+        hen = tc < ee ? a.centry[tc] : ~uint64_t(0);
+      }
+      element_terms(be, a.h2, kk, L0, K, F);
     }
     if (live) {
       st_block(a.vals, int64_t(ob) + p, K);
@@ -534,6 +542,25 @@ assemble_rows(AsmArgs a) {
     Fs[0] += F[0];
     Fs[1] += F[1];
     Fs[2] += F[2];
+    // step the column cursors to the lane's next block (d slots on); with no
+    // new column left the spring cursor jumps
+    const int32_t kn = k + kRowLanes;
+    int32_t d = kn + (kn >= dpos) - p;
+    while (d > 0) {
+      if (ht == kEnd) {
+        sc += d;
+        break;
+      }
+      if (hs < ht) {
+        ++sc;
+        hs = sc < nS ? S[sc] : kEnd;
+      } else {
+        ++tn;
+        ht = tn < nT ? T[tn] : kEnd;
+      }
+      --d;
+    }
+    hs = sc < nS ? S[sc] : kEnd;
   }
   // merge the lanes' partials: TwoSum's error is the exact rounding error of
   // the sum, so both lanes of a pair get the same bits in either order
@@ -622,7 +649,7 @@ int assemble_system(Handle* h, const float* x, const float* v,
     contact_scatter<<<cgrid, 256, 0, s>>>(nc, n, contacts->i, contacts->j, rowcnt, fill,
                                           centry);
     row_classify<<<rgrid, 256, 0, s>>>(n, rowcnt, centry, h->rowptr_s, h->colind_s, h->newcol,
-                                       h->newfirst, h->newcnt);
+                                       h->newcnt);
     h->launches += 2;
     rc = scan_exclusive(h, h->newcnt, n + 1, h->counters);
     if (rc != PCLOTH_OK) return rc;
@@ -630,7 +657,6 @@ int assemble_system(Handle* h, const float* x, const float* v,
     a.nbefore = h->newcnt;
     a.centry = centry;
     a.newcol = h->newcol;
-    a.newfirst = h->newfirst;
     a.ck = contacts->k;
     a.cr = contacts->rest;
   }

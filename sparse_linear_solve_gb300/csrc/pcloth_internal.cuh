@@ -134,7 +134,6 @@ struct Handle {
                                    // entry of each row; then the scatter cursors
   int32_t* newcnt = nullptr;       // [n+1]: new blocks per row, scanned to those before it
   int32_t* newcol = nullptr;       // a row's new columns, at its first entry's index
-  int32_t* newfirst = nullptr;     // first entry of each new column
   int32_t* counters = nullptr;     // [0] = #new blocks, [1] = #valid entries, [2] pairs
 
   // host-input staging for pcloth_step_host

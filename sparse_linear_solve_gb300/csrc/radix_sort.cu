@@ -7,7 +7,9 @@
 // over one 8-bit digit is three kernels: per-tile digit histograms, one
 // exclusive scan of the digit-major histogram table, and a stable scatter
 // that ranks keys inside each warp with match_any.  The scan also serves
-// the assembly's per-row counts (assemble.cu).
+// the assembly's per-row counts (assemble.cu): per-tile sums, then each
+// tile's scan plus its offset, which the tile adds up from the sums before
+// it (up to 1024 tiles; larger scans scan the sums in a launch of their own).
 
 #include "pcloth_internal.cuh"
 
@@ -206,6 +208,37 @@ scan_tiles_apply(int32_t* __restrict__ data, int32_t n, const int32_t* __restric
     if (base + k < n) data[base + k] = v[k] + o;
 }
 
+// The tile's exclusive scan plus its offset, the sum of the totals of the
+// tiles before it, which the block adds up itself (at most kInlineTiles of
+// them, read from L2): the single-block scan of the tile totals and its
+// launch are saved.  The last block writes the grand total.
+constexpr int kInlineTiles = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+scan_tiles_apply_inline(int32_t* __restrict__ data, int32_t n,
+                        const int32_t* __restrict__ sums, int32_t* __restrict__ total) {
+  __shared__ int32_t wsum[33];
+  __shared__ int32_t red[kScanThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t part = 0;
+  for (int b = threadIdx.x; b < int(blockIdx.x); b += kScanThreads) part += sums[b];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(0xffffffffu, part, o);
+  if (lane == 0) red[warp] = part;
+  int32_t v[kScanItems];
+  const int64_t base = int64_t(blockIdx.x) * kScanTile + int64_t(threadIdx.x) * kScanItems;
+#pragma unroll
+  for (int k = 0; k < kScanItems; ++k) v[k] = (base + k < n) ? data[base + k] : 0;
+  const int32_t tot = block_scan_items(v, wsum);   // synchronises the block: red[] is complete
+  int32_t off = 0;
+#pragma unroll
+  for (int w = 0; w < kScanThreads / 32; ++w) off += red[w];
+#pragma unroll
+  for (int k = 0; k < kScanItems; ++k)
+    if (base + k < n) data[base + k] = v[k] + off;
+  if (total && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) *total = off + tot;
+}
+
 }  // namespace
 
 int radix_sort_pairs(Handle* h, uint64_t* keys[2], int32_t* vals[2], int32_t n,
@@ -239,6 +272,12 @@ int scan_exclusive(Handle* h, int32_t* data, int32_t n, int32_t* total_dev) {
     return check_launch(h, "scan");
   }
   scan_tile_sums<<<ntiles, kScanThreads, 0, h->stream>>>(data, n, h->scan_tmp);
+  if (ntiles <= kInlineTiles) {
+    scan_tiles_apply_inline<<<ntiles, kScanThreads, 0, h->stream>>>(data, n, h->scan_tmp,
+                                                                   total_dev);
+    h->launches += 2;
+    return check_launch(h, "scan");
+  }
   scan_one_block<<<1, 1024, 0, h->stream>>>(h->scan_tmp, ntiles, total_dev);
   scan_tiles_apply<<<ntiles, kScanThreads, 0, h->stream>>>(data, n, h->scan_tmp);
   h->launches += 3;
