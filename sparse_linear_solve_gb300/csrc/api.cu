@@ -34,13 +34,13 @@ void free_handle(Handle* h) {
   cudaStreamSynchronize(h->stream);
   void* bufs[] = {h->mass, h->rowptr_s, h->colind_s, h->sblk_ptr, h->sentry,
                   h->rowptr, h->colind, h->vals, h->rhs, h->vec_arena,
-                  h->ckey[0], h->ckey[1], h->cval[0], h->cval[1],
-                  h->sort_counts, h->scan_tmp, h->rowcnt, h->newcnt, h->newcol,
+                  h->centry, h->hash_first, h->hash_where, h->hash_slot, h->pair_first,
+                  h->scan_tmp, h->rowcnt, h->newcnt, h->newcol,
                   h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
                   h->dv, h->rec, h->bar,
                   h->phase_ns, h->state, h->d_status, h->bell_wmax, h->bell_col, h->bell_val,
-                  h->vkey[0], h->vkey[1], h->vid[0], h->vid[1]};
+                  };
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (h->state_host) cudaFreeHost(h->state_host);
@@ -51,11 +51,6 @@ void free_handle(Handle* h) {
   delete h;
 }
 
-int bits_for(int64_t n) {  // smallest b with 2^b > n
-  int b = 1;
-  while ((int64_t(1) << b) <= n) ++b;
-  return b;
-}
 }  // namespace
 
 namespace pcloth_impl {
@@ -130,7 +125,6 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   h->ns = int32_t(ns);
   h->max_contacts = int32_t(mc);
   for (int c = 0; c < 3; ++c) h->gravity[c] = mesh->gravity[c];
-  h->key_bits = bits_for(n);
   h->nnzb_cap = cap;
   cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
   if (h->sm_count <= 0) h->sm_count = 1;
@@ -201,10 +195,15 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
 
   // ---- device buffers ---------------------------------------------------
   const int64_t ent2 = std::max<int64_t>(2 * mc, 1);
-  // the radix sort also orders the n vertices by cell for contact finding
-  const int64_t sort_tiles = (std::max<int64_t>(ent2, n) + kSortTile - 1) / kSortTile;
-  // scans run over the n + 1 per-row counts of the assembly
-  const int64_t scan_tiles = (std::max<int64_t>(ent2, n + 1) + kScanTile - 1) / kScanTile;
+  // contact finding hashes cells into a power-of-two table of at least 2n
+  // buckets
+  int64_t buckets = 1024;
+  while (buckets < 2 * n) buckets *= 2;
+  h->hash_mask = uint32_t(buckets - 1);
+  // scans run over the n + 1 per-row counts of the assembly, the n + 1
+  // per-vertex pair counts and the buckets + 1 hash counts
+  const int64_t scan_tiles =
+      (std::max<int64_t>(ent2, buckets + 1) + kScanTile - 1) / kScanTile;
   h->spmv_grid = spmv_grid_for(int32_t(n), h->sm_count);
   {
     const int ge = pcg_loop_grid(kSymBlock, int32_t(n), h->device, h->sm_count, &h->loop_grid);
@@ -258,13 +257,11 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
       h->pinv6 = reinterpret_cast<float*>(base + off[5]);
     }
   }
-  for (int b = 0; b < 2; ++b) {
-    A(dalloc(&h->ckey[b], ent2));
-    A(dalloc(&h->cval[b], ent2));
-    A(dalloc(&h->vkey[b], n));
-    A(dalloc(&h->vid[b], n));
-  }
-  A(dalloc(&h->sort_counts, sort_tiles * kSortRadix + 1));
+  A(dalloc(&h->centry, ent2));
+  A(dalloc(&h->hash_first, buckets + 1));
+  A(dalloc(&h->hash_where, n));
+  A(dalloc(&h->hash_slot, n));
+  A(dalloc(&h->pair_first, n + 1));
   A(dalloc(&h->scan_tmp, scan_tiles + 1));
   A(dalloc(&h->rowcnt, 2 * (n + 1)));
   A(dalloc(&h->newcnt, n + 1));

@@ -637,7 +637,7 @@ int assemble_system(Handle* h, const float* x, const float* v,
   if (nc > 0) {
     int32_t* rowcnt = h->rowcnt;          // [n+1]: counts, then first entry per row
     int32_t* fill = h->rowcnt + (n + 1);  // [n+1]: scatter cursors
-    uint64_t* centry = h->ckey[0];
+    uint64_t* centry = h->centry;
     cudaError_t e = cudaMemsetAsync(h->rowcnt, 0, 2 * (size_t(n) + 1) * sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(h, e, "contact counts reset");
     const int cgrid = (nc + 255) / 256, rgrid = (n + 1 + 255) / 256;

@@ -5,20 +5,25 @@
 // a radius r that is not a spring becomes a contact (a spring of stiffness
 // k_c and rest length r), listed in (i, j) order.
 //
-//   cell_keys     each vertex to its cell of edge r (1 + 2^-7): the slight
+//   hash_count    each vertex to its cell of edge r (1 + 2^-7): the slight
 //                 enlargement keeps every pair closer than r in neighbouring
 //                 cells despite the rounding of x / edge, for coordinates up
-//                 to 2^15 cells from the origin (65 m at r = 2 mm)
-//   radix sort    vertices by cell key (z fastest, so the three cells of a
-//                 column along z are contiguous in key order)
-//   find_pairs    per vertex: the 3 x 3 columns of neighbouring cells, one
-//                 binary search each; every candidate j > i gets the exact
-//                 test in float32 ((dx dx + dy dy) + dz dz < r r, each
-//                 operation rounded) and spring pairs are dropped by a
-//                 binary search in the static pattern; survivors are
-//                 appended
-//   radix sort    the appended (i, j) keys, so the list is deterministic
-//   unpack        into the caller's i, j, k, rest arrays
+//                 to 2^15 cells from the origin (65 m at r = 2 mm); the cell
+//                 to a bucket of a table of T >= 2n buckets by the hash of
+//                 Teschner et al. (2003, "Optimized Spatial Hashing for
+//                 Collision Detection of Deformable Objects"), counted with
+//                 an atomic that also gives the vertex its place in the bucket
+//   scan          the buckets' first slots
+//   hash_fill     each vertex's position and index into its bucket's slot
+//   pair_pass     per vertex i, twice: the 27 buckets of the cells around
+//                 its own; a candidate j > i counts if it lies in that very
+//                 cell (buckets are shared by colliding cells), passes the
+//                 exact float32 test ((dx dx + dy dy) + dz dz < r r, each
+//                 operation rounded) and is no spring (a binary search in
+//                 the static pattern).  The first pass counts, a scan gives
+//                 every vertex its first output slot, and the second pass
+//                 writes the partners and sorts them, so the list comes out
+//                 in (i, j) order whatever the order inside the buckets.
 //
 // The distance test decides an integer outcome, so it is written with
 // explicitly rounded operations (no fused multiply-add) to be reproducible
@@ -31,39 +36,38 @@
 namespace pcloth_impl {
 namespace {
 
-constexpr int kCellBits = 21;                          // per axis
-constexpr int32_t kCellBias = 1 << (kCellBits - 1);    // cells -2^20 .. 2^20 - 1
-constexpr uint64_t kCellMask = (uint64_t(1) << kCellBits) - 1;
-
-__device__ __forceinline__ uint64_t cell_key(int32_t cx, int32_t cy, int32_t cz) {
-  return (uint64_t(uint32_t(cx + kCellBias) & kCellMask) << (2 * kCellBits)) |
-         (uint64_t(uint32_t(cy + kCellBias) & kCellMask) << kCellBits) |
-         uint64_t(uint32_t(cz + kCellBias) & kCellMask);
-}
+constexpr int32_t kCellLimit = 1 << 20;   // cells clamped to [-2^20 + 2, 2^20 - 3]
 
 __device__ __forceinline__ int32_t cell_of(float v, float inv_edge) {
   const float c = floorf(v * inv_edge);
-  return int32_t(fminf(fmaxf(c, float(-kCellBias + 2)), float(kCellBias - 3)));
+  return int32_t(fminf(fmaxf(c, float(-kCellLimit + 2)), float(kCellLimit - 3)));
 }
 
-__global__ void cell_keys(int32_t n, const float* __restrict__ x, float inv_edge,
-                          uint64_t* __restrict__ keys, int32_t* __restrict__ ids,
-                          uint32_t* status) {
+// Teschner et al.'s spatial hash: the cell's coordinates times three large
+// primes, combined by exclusive or, modulo the table size (a power of two).
+__device__ __forceinline__ uint32_t cell_hash(int32_t cx, int32_t cy, int32_t cz, uint32_t mask) {
+  return ((uint32_t(cx) * 73856093u) ^ (uint32_t(cy) * 19349663u) ^ (uint32_t(cz) * 83492791u)) &
+         mask;
+}
+
+__global__ void hash_count(int32_t n, const float* __restrict__ x, float inv_edge, uint32_t mask,
+                           int32_t* __restrict__ count, int2* __restrict__ where,
+                           uint32_t* status) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const float px = x[3 * i], py = x[3 * i + 1], pz = x[3 * i + 2];
   if (!finite3(px, py, pz)) atomicOr(status, ST_NONFINITE);
-  keys[i] = cell_key(cell_of(px, inv_edge), cell_of(py, inv_edge), cell_of(pz, inv_edge));
-  ids[i] = int32_t(i);
+  const uint32_t b =
+      cell_hash(cell_of(px, inv_edge), cell_of(py, inv_edge), cell_of(pz, inv_edge), mask);
+  where[i] = make_int2(int32_t(b), atomicAdd(&count[b], 1));
 }
 
-__device__ __forceinline__ int32_t lower_bound_u64(const uint64_t* a, int32_t n, uint64_t v) {
-  int32_t lo = 0, hi = n;
-  while (lo < hi) {
-    const int32_t mid = (lo + hi) >> 1;
-    if (a[mid] < v) lo = mid + 1; else hi = mid;
-  }
-  return lo;
+__global__ void hash_fill(int32_t n, const float* __restrict__ x, const int2* __restrict__ where,
+                          const int32_t* __restrict__ first, float4* __restrict__ slot) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int2 w = where[i];
+  slot[first[w.x] + w.y] = make_float4(x[3 * i], x[3 * i + 1], x[3 * i + 2], __int_as_float(int32_t(i)));
 }
 
 __device__ __forceinline__ bool is_spring(const int32_t* __restrict__ rowptr_s,
@@ -79,52 +83,107 @@ __device__ __forceinline__ bool is_spring(const int32_t* __restrict__ rowptr_s,
   return false;
 }
 
-// One thread per sorted position t (vertex i = ids[t]).
-__global__ void find_pairs(int32_t n, const float* __restrict__ x, float r2, float inv_edge,
-                           const uint64_t* __restrict__ keys, const int32_t* __restrict__ ids,
-                           const int32_t* __restrict__ rowptr_s,
-                           const int32_t* __restrict__ colind_s, int key_bits,
-                           unsigned long long* __restrict__ pairs, int32_t capacity,
-                           int32_t* counter) {
-  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= n) return;
-  const int32_t i = ids[t];
-  const float px = x[3 * int64_t(i)], py = x[3 * int64_t(i) + 1], pz = x[3 * int64_t(i) + 2];
-  const int32_t cx = cell_of(px, inv_edge), cy = cell_of(py, inv_edge), cz = cell_of(pz, inv_edge);
-  for (int ox = -1; ox <= 1; ++ox) {
-    for (int oy = -1; oy <= 1; ++oy) {
-      const int32_t b = lower_bound_u64(keys, n, cell_key(cx + ox, cy + oy, cz - 1));
-      const uint64_t last = cell_key(cx + ox, cy + oy, cz + 1);
-      for (int32_t u = b; u < n && keys[u] <= last; ++u) {
-        const int32_t j = ids[u];
-        if (j <= i) continue;
-        const float dx = __fsub_rn(x[3 * int64_t(j)], px);
-        const float dy = __fsub_rn(x[3 * int64_t(j) + 1], py);
-        const float dz = __fsub_rn(x[3 * int64_t(j) + 2], pz);
-        const float d2 = __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)),
-                                   __fmul_rn(dz, dz));
-        if (!(d2 < r2)) continue;
-        if (is_spring(rowptr_s, colind_s, i, j)) continue;
-        const int32_t slot = atomicAdd(counter, 1);
-        if (slot < capacity)
-          pairs[slot] = (static_cast<unsigned long long>(i) << key_bits) |
-                        static_cast<unsigned long long>(j);
+// Sorts a vertex's few partners in place: insertion sort, or heapsort for
+// many (a vertex inside a dense cluster).
+__device__ void sort_partners(int32_t* a, int32_t m) {
+  if (m <= 32) {
+    for (int32_t t = 1; t < m; ++t) {
+      const int32_t key = a[t];
+      int32_t u = t - 1;
+      while (u >= 0 && a[u] > key) {
+        a[u + 1] = a[u];
+        --u;
       }
+      a[u + 1] = key;
     }
+    return;
+  }
+  auto sift = [&](int32_t root, int32_t end) {   // max-heap on [0, end)
+    while (true) {
+      int32_t child = 2 * root + 1;
+      if (child >= end) return;
+      if (child + 1 < end && a[child + 1] > a[child]) ++child;
+      if (a[root] >= a[child]) return;
+      const int32_t t = a[root];
+      a[root] = a[child];
+      a[child] = t;
+      root = child;
+    }
+  };
+  for (int32_t r = m / 2 - 1; r >= 0; --r) sift(r, m);
+  for (int32_t end = m - 1; end > 0; --end) {
+    const int32_t t = a[0];
+    a[0] = a[end];
+    a[end] = t;
+    sift(0, end);
   }
 }
 
-__global__ void unpack_pairs(int32_t m, const uint64_t* __restrict__ pairs, int key_bits,
-                             float k, float rest, int32_t* __restrict__ oi,
-                             int32_t* __restrict__ oj, float* __restrict__ ok,
-                             float* __restrict__ orest) {
+struct PairArgs {
+  int32_t n;
+  float r2, inv_edge;
+  uint32_t mask;
+  const float* x;
+  const int32_t* first;    // [T + 1] first slot of each bucket
+  const float4* slot;      // [n] (x, y, z, index) in bucket order
+  const int32_t* rowptr_s;
+  const int32_t* colind_s;
+  int32_t* count;          // count pass: partners of each vertex
+  const int32_t* out_first;  // write pass: each vertex's first output slot
+  int32_t* oi;
+  int32_t* oj;
+  float* ok;
+  float* orest;
+  float k, rest;
+};
+
+template <bool kWrite>
+__global__ void pair_pass(PairArgs a) {
   const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= m) return;
-  const uint64_t p = pairs[t];
-  oi[t] = int32_t(p >> key_bits);
-  oj[t] = int32_t(p & ((uint64_t(1) << key_bits) - 1));
-  ok[t] = k;
-  orest[t] = rest;
+  if (t >= a.n) return;
+  const int32_t i = int32_t(t);
+  const float px = a.x[3 * t], py = a.x[3 * t + 1], pz = a.x[3 * t + 2];
+  const int32_t cx = cell_of(px, a.inv_edge), cy = cell_of(py, a.inv_edge);
+  const int32_t cz = cell_of(pz, a.inv_edge);
+  const int32_t base = kWrite ? a.out_first[i] : 0;
+  int32_t c = 0;
+  for (int ox = -1; ox <= 1; ++ox) {
+    for (int oy = -1; oy <= 1; ++oy) {
+      for (int oz = -1; oz <= 1; ++oz) {
+        const int32_t nx = cx + ox, ny = cy + oy, nz = cz + oz;
+        const uint32_t b = cell_hash(nx, ny, nz, a.mask);
+        const int32_t u1 = a.first[b + 1];
+        for (int32_t u = a.first[b]; u < u1; ++u) {
+          const float4 s = a.slot[u];
+          const int32_t j = __float_as_int(s.w);
+          if (j <= i) continue;
+          if (cell_of(s.x, a.inv_edge) != nx || cell_of(s.y, a.inv_edge) != ny ||
+              cell_of(s.z, a.inv_edge) != nz)
+            continue;   // another cell with the same hash
+          const float dx = __fsub_rn(s.x, px);
+          const float dy = __fsub_rn(s.y, py);
+          const float dz = __fsub_rn(s.z, pz);
+          const float d2 = __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)),
+                                     __fmul_rn(dz, dz));
+          if (!(d2 < a.r2)) continue;
+          if (is_spring(a.rowptr_s, a.colind_s, i, j)) continue;
+          if (kWrite) a.oj[base + c] = j;
+          ++c;
+        }
+      }
+    }
+  }
+  if (!kWrite) {
+    a.count[i] = c;
+    if (i == a.n - 1) a.count[a.n] = 0;   // the scan's total slot
+    return;
+  }
+  sort_partners(a.oj + base, c);
+  for (int32_t q = 0; q < c; ++q) {
+    a.oi[base + q] = i;
+    a.ok[base + q] = a.k;
+    a.orest[base + q] = a.rest;
+  }
 }
 
 }  // namespace
@@ -136,43 +195,62 @@ int find_contacts(Handle* h, const float* x, float radius, float stiffness,
   const float edge = radius * (1.0f + 1.0f / 128.0f);
   const float inv_edge = 1.0f / edge;
   const float r2 = radius * radius;   // float32, as the test compares
-  // vertices by cell
-  cell_keys<<<(n + 255) / 256, 256, 0, s>>>(n, x, inv_edge, h->vkey[0], h->vid[0], h->d_status);
+  const int32_t nb = int32_t(h->hash_mask) + 1;   // buckets
+  const int grid = (n + 255) / 256;
+  // the hash table: bucket counts, their scan, the vertices in bucket order
+  cudaError_t e = cudaMemsetAsync(h->hash_first, 0, (size_t(nb) + 1) * sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "hash table reset");
+  hash_count<<<grid, 256, 0, s>>>(n, x, inv_edge, h->hash_mask, h->hash_first, h->hash_where,
+                                  h->d_status);
   h->launches += 1;
-  int rc = check_launch(h, "cell keys");
+  int rc = check_launch(h, "hash count");
   if (rc != PCLOTH_OK) return rc;
-  const int cur = radix_sort_pairs(h, h->vkey, h->vid, n, 3 * 21);
-  if (cur < 0) return cur;
-  // candidate pairs, appended
-  cudaError_t e = cudaMemsetAsync(h->counters + 2, 0, sizeof(int32_t), s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "pair counter");
-  const int32_t cap = std::min<int32_t>(capacity, h->max_contacts);
-  find_pairs<<<(n + 255) / 256, 256, 0, s>>>(
-      n, x, r2, inv_edge, h->vkey[cur], h->vid[cur], h->rowptr_s, h->colind_s, h->key_bits,
-      reinterpret_cast<unsigned long long*>(h->ckey[0]), cap, h->counters + 2);
+  rc = scan_exclusive(h, h->hash_first, nb + 1, h->counters + 2);
+  if (rc != PCLOTH_OK) return rc;
+  hash_fill<<<grid, 256, 0, s>>>(n, x, h->hash_where, h->hash_first, h->hash_slot);
   h->launches += 1;
-  rc = check_launch(h, "find pairs");
+  rc = check_launch(h, "hash fill");
+  if (rc != PCLOTH_OK) return rc;
+  // partners per vertex, their scan, and the total on the host
+  PairArgs a{};
+  a.n = n;
+  a.r2 = r2;
+  a.inv_edge = inv_edge;
+  a.mask = h->hash_mask;
+  a.x = x;
+  a.first = h->hash_first;
+  a.slot = h->hash_slot;
+  a.rowptr_s = h->rowptr_s;
+  a.colind_s = h->colind_s;
+  a.count = h->pair_first;
+  pair_pass<false><<<grid, 256, 0, s>>>(a);
+  h->launches += 1;
+  rc = check_launch(h, "pair count");
+  if (rc != PCLOTH_OK) return rc;
+  rc = scan_exclusive(h, h->pair_first, n + 1, h->counters + 2);
   if (rc != PCLOTH_OK) return rc;
   int32_t total = 0;
   e = cudaMemcpyAsync(&total, h->counters + 2, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(h, e, "pair count");
   if (found) *found = total;
+  const int32_t cap = std::min<int32_t>(capacity, h->max_contacts);
   if (total > cap) {
     out->n = 0;
     return fail(h, PCLOTH_ERR_CAPACITY,
                 "found " + std::to_string(total) + " contacts, capacity " + std::to_string(cap));
   }
-  // (i, j) order
-  const int cur2 = radix_sort_pairs(h, h->ckey, h->cval, total, 2 * h->key_bits);
-  if (cur2 < 0) return cur2;
   if (total > 0) {
-    unpack_pairs<<<(total + 255) / 256, 256, 0, s>>>(
-        total, h->ckey[cur2], h->key_bits, stiffness, radius, const_cast<int32_t*>(out->i),
-        const_cast<int32_t*>(out->j), const_cast<float*>(out->k),
-        const_cast<float*>(out->rest));
+    a.out_first = h->pair_first;
+    a.oi = const_cast<int32_t*>(out->i);
+    a.oj = const_cast<int32_t*>(out->j);
+    a.ok = const_cast<float*>(out->k);
+    a.orest = const_cast<float*>(out->rest);
+    a.k = stiffness;
+    a.rest = radius;
+    pair_pass<true><<<grid, 256, 0, s>>>(a);
     h->launches += 1;
-    rc = check_launch(h, "unpack pairs");
+    rc = check_launch(h, "pair write");
     if (rc != PCLOTH_OK) return rc;
   }
   out->n = total;

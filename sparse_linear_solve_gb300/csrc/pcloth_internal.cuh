@@ -34,12 +34,6 @@ struct PcgState {
 };
 
 // ------------------------------------------------------------ sizes --------
-constexpr int kSortBits = 8;                 // radix digit width
-constexpr int kSortRadix = 1 << kSortBits;
-constexpr int kSortThreads = 256;
-constexpr int kSortItems = 8;                // keys per thread per tile
-constexpr int kSortTile = kSortThreads * kSortItems;
-
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;
@@ -90,7 +84,6 @@ struct Handle {
   int32_t n = 0;             // vertices
   int32_t ns = 0;            // springs
   int32_t max_contacts = 0;
-  int key_bits = 1;          // bits per vertex index in a sort key
   int64_t nnzb_static = 0;
   int64_t nnzb_cap = 0;
   float gravity[3] = {0, 0, 0};
@@ -123,12 +116,9 @@ struct Handle {
   float* pinv6 = nullptr;        // [6][vstride] planes P00 P01 P02 P11 P12 P22
 
   // per-step contact workspace (capacity 2*max_contacts entries).  The
-  // assembly buckets a step's contact entries by row: ckey[0] holds them,
-  // per row sorted by (column << 32 | contact id); ckey/cval are also the
-  // radix sort's buffers for contact finding.
-  uint64_t* ckey[2] = {nullptr, nullptr};
-  int32_t* cval[2] = {nullptr, nullptr};
-  int32_t* sort_counts = nullptr;  // radix * tiles
+  // assembly buckets a step's contact entries by row: centry holds them,
+  // per row sorted by (column << 32 | contact id).
+  uint64_t* centry = nullptr;
   int32_t* scan_tmp = nullptr;     // per-tile sums
   int32_t* rowcnt = nullptr;       // [2(n+1)]: entries per row, scanned to the first
                                    // entry of each row; then the scatter cursors
@@ -166,9 +156,12 @@ struct Handle {
   uint32_t* d_status = nullptr;    // device error bits
   uint32_t* h_status = nullptr;    // pinned copy
 
-  // contact finding: vertices sorted by spatial-hash cell
-  uint64_t* vkey[2] = {nullptr, nullptr};   // n
-  int32_t* vid[2] = {nullptr, nullptr};     // n
+  // contact finding: a spatial-hash table of hash_mask + 1 buckets
+  uint32_t hash_mask = 0;
+  int32_t* hash_first = nullptr;   // [buckets + 1]: counts, scanned to each bucket's first slot
+  int2* hash_where = nullptr;      // [n]: each vertex's bucket and place in it
+  float4* hash_slot = nullptr;     // [n]: (x, y, z, index) in bucket order
+  int32_t* pair_first = nullptr;   // [n + 1]: partners per vertex, scanned to first output
 
   // block-ELL copy of the assembled matrix (the pages' layout), built on
   // request for the head-to-head SpMV; invalid after the next assembly
@@ -190,12 +183,8 @@ int cuda_fail(Handle* h, cudaError_t e, const char* what);
 int check_launch(Handle* h, const char* what);
 int collect_status(Handle* h);  // sync + read d_status; returns error code
 
-// radix_sort.cu
-// Stable LSD sort of (key, val) pairs on the low `bits` bits of the keys.
-// Ping-pong between buffers 0 and 1; returns the index holding the result.
-int radix_sort_pairs(Handle* h, uint64_t* keys[2], int32_t* vals[2], int32_t n,
-                     int bits);
-// Exclusive scan of int32 flags in place; writes the total to *total_dev.
+// scan.cu
+// Exclusive scan of int32 counts in place; writes the total to *total_dev.
 int scan_exclusive(Handle* h, int32_t* data, int32_t n, int32_t* total_dev);
 
 // assemble.cu

@@ -1,39 +1,14 @@
-// Stable LSD radix sort of (uint64 key, int32 value) pairs and an exclusive
-// int32 scan.
-//
-// The sort orders the vertices by spatial-hash cell and the found contact
-// pairs by (i, j) for contact finding (contacts.cu; P-Cloth Sec. 4.2): equal
-// keys keep their input order, so the results are deterministic.  Each pass
-// over one 8-bit digit is three kernels: per-tile digit histograms, one
-// exclusive scan of the digit-major histogram table, and a stable scatter
-// that ranks keys inside each warp with match_any.  The scan also serves
-// the assembly's per-row counts (assemble.cu): per-tile sums, then each
-// tile's scan plus its offset, which the tile adds up from the sums before
-// it (up to 1024 tiles; larger scans scan the sums in a launch of their own).
+// Exclusive scans of int32 counts, in place: the assembly's per-row contact
+// entries and new blocks (assemble.cu) and the contact finder's bucket and
+// pair counts (contacts.cu).  Two launches: per-tile sums, then each tile's
+// scan plus its offset, which the tile adds up itself from the sums before
+// it (up to kInlineTiles tiles; a longer scan scans the sums in a launch of
+// its own, between the two).
 
 #include "pcloth_internal.cuh"
 
 namespace pcloth_impl {
 namespace {
-
-constexpr int kWarps = kSortThreads / 32;
-
-__global__ void __launch_bounds__(kSortThreads)
-rs_upsweep(const uint64_t* __restrict__ keys, int32_t n, int shift,
-           int32_t* __restrict__ counts, int ntiles) {
-  __shared__ int32_t hist[kSortRadix];
-  for (int d = threadIdx.x; d < kSortRadix; d += kSortThreads) hist[d] = 0;
-  __syncthreads();
-  const int64_t base = int64_t(blockIdx.x) * kSortTile;
-#pragma unroll
-  for (int it = 0; it < kSortItems; ++it) {
-    const int64_t idx = base + it * kSortThreads + threadIdx.x;
-    if (idx < n) atomicAdd(&hist[int((keys[idx] >> shift) & (kSortRadix - 1))], 1);
-  }
-  __syncthreads();
-  for (int d = threadIdx.x; d < kSortRadix; d += kSortThreads)
-    counts[int64_t(d) * ntiles + blockIdx.x] = hist[d];
-}
 
 // Exclusive scan of data[0, n) by a single block of 1024 threads, carrying a
 // running total across chunks of 4096 values.  Writes the grand total to
@@ -84,63 +59,6 @@ scan_one_block(int32_t* __restrict__ data, int32_t n, int32_t* __restrict__ tota
     __syncthreads();
   }
   if (threadIdx.x == 0 && total) *total = carry;
-}
-
-__global__ void __launch_bounds__(kSortThreads)
-rs_downsweep(const uint64_t* __restrict__ kin, const int32_t* __restrict__ vin,
-             uint64_t* __restrict__ kout, int32_t* __restrict__ vout, int32_t n,
-             int shift, const int32_t* __restrict__ offsets, int ntiles) {
-  __shared__ int32_t whist[kWarps][kSortRadix];
-  __shared__ int32_t toff[kSortRadix];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int d = threadIdx.x; d < kSortRadix; d += kSortThreads) {
-    toff[d] = offsets[int64_t(d) * ntiles + blockIdx.x];
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) whist[w][d] = 0;
-  }
-  __syncthreads();
-  const int64_t wbase = int64_t(blockIdx.x) * kSortTile + warp * (32 * kSortItems);
-  uint64_t key[kSortItems];
-  int32_t val[kSortItems];
-  int dig[kSortItems];
-  int rank[kSortItems];
-  const unsigned lt_mask = (1u << lane) - 1u;
-#pragma unroll
-  for (int it = 0; it < kSortItems; ++it) {
-    const int64_t idx = wbase + it * 32 + lane;
-    const bool valid = idx < n;
-    key[it] = valid ? kin[idx] : 0ull;
-    val[it] = valid ? vin[idx] : 0;
-    dig[it] = valid ? int((key[it] >> shift) & (kSortRadix - 1)) : kSortRadix;
-    const unsigned peers = __match_any_sync(0xffffffffu, dig[it]);
-    const int leader = __ffs(peers) - 1;
-    int base = 0;
-    if (valid) base = whist[warp][dig[it]];
-    __syncwarp();
-    if (valid && lane == leader) whist[warp][dig[it]] = base + __popc(peers);
-    __syncwarp();
-    rank[it] = base + __popc(peers & lt_mask);
-  }
-  __syncthreads();
-  // exclusive scan across warps, per digit
-  for (int d = threadIdx.x; d < kSortRadix; d += kSortThreads) {
-    int32_t run = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int32_t t = whist[w][d];
-      whist[w][d] = run;
-      run += t;
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int it = 0; it < kSortItems; ++it) {
-    if (dig[it] < kSortRadix) {
-      const int64_t pos = int64_t(toff[dig[it]]) + whist[warp][dig[it]] + rank[it];
-      kout[pos] = key[it];
-      vout[pos] = val[it];
-    }
-  }
 }
 
 // Exclusive block scan of kScanItems values per thread; returns the block
@@ -212,7 +130,7 @@ scan_tiles_apply(int32_t* __restrict__ data, int32_t n, const int32_t* __restric
 // tiles before it, which the block adds up itself (at most kInlineTiles of
 // them, read from L2): the single-block scan of the tile totals and its
 // launch are saved.  The last block writes the grand total.
-constexpr int kInlineTiles = 1024;
+constexpr int kInlineTiles = 2048;
 
 __global__ void __launch_bounds__(kScanThreads)
 scan_tiles_apply_inline(int32_t* __restrict__ data, int32_t n,
@@ -240,25 +158,6 @@ scan_tiles_apply_inline(int32_t* __restrict__ data, int32_t n,
 }
 
 }  // namespace
-
-int radix_sort_pairs(Handle* h, uint64_t* keys[2], int32_t* vals[2], int32_t n,
-                     int bits) {
-  int cur = 0;
-  if (n <= 1) return cur;
-  const int ntiles = (n + kSortTile - 1) / kSortTile;
-  for (int shift = 0; shift < bits; shift += kSortBits) {
-    rs_upsweep<<<ntiles, kSortThreads, 0, h->stream>>>(keys[cur], n, shift,
-                                                       h->sort_counts, ntiles);
-    scan_one_block<<<1, 1024, 0, h->stream>>>(h->sort_counts, kSortRadix * ntiles, nullptr);
-    rs_downsweep<<<ntiles, kSortThreads, 0, h->stream>>>(
-        keys[cur], vals[cur], keys[cur ^ 1], vals[cur ^ 1], n, shift,
-        h->sort_counts, ntiles);
-    h->launches += 3;
-    cur ^= 1;
-  }
-  int rc = check_launch(h, "radix sort");
-  return rc == PCLOTH_OK ? cur : rc;
-}
 
 int scan_exclusive(Handle* h, int32_t* data, int32_t n, int32_t* total_dev) {
   if (n <= 0) {

@@ -110,6 +110,34 @@ def test_contacts_duplicates_and_spring_pairs():
     compare_assembly(w, w.x0, w.v0, c)
 
 
+def test_rows_with_new_blocks_on_both_sides_of_the_diagonal():
+    """Rows whose new (contact) columns interleave with their spring columns
+    below and above the diagonal, with several contacts on one block, on
+    spring blocks and on new blocks: the assembly's lanes find every block's
+    column and contact run by walking the row (filling steps 1-3), so each
+    row's pattern must still come out bit-exact and its values match."""
+    w = W.tiny_cloth(n=16, rest_from_grid=True)
+    rng = np.random.default_rng(7)
+    nv = w.n_verts
+    ci, cj = [], []
+    for hub in (17, 60, 119, 120, 201, 254):
+        springs = np.concatenate([w.spring_j[w.spring_i == hub], w.spring_i[w.spring_j == hub]])
+        others = rng.choice(nv, size=10, replace=False)
+        partners = [int(o) for o in others if o != hub] + [int(springs[0]), int(springs[-1])]
+        partners += partners[:3]   # repeated contacts on the same block
+        for q, j in enumerate(partners):
+            # both orientations of the pair, as callers may list either
+            ci.append(hub if q % 2 == 0 else j)
+            cj.append(j if q % 2 == 0 else hub)
+    ci, cj = np.array(ci, np.int32), np.array(cj, np.int32)
+    nc = len(ci)
+    ck = rng.uniform(1e2, 1e3, nc).astype(np.float32)
+    cr = rng.uniform(1e-3, 5e-3, nc).astype(np.float32)
+    c = W.Contacts(ci, cj, ck, cr)
+    w.max_contacts = nc
+    compare_assembly(w, w.x0, w.v0, c)
+
+
 def test_long_rows_exercise_chunked_paths():
     """One vertex in contact with 1500 others: its row is longer than the
     assembly staging and the SpMV chunk, and a tile exceeds both.  Soft
