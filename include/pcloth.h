@@ -135,7 +135,8 @@ int pcloth_spmv(pcloth_t h, const float* in, float* out);
  * written in (i, j) order into the caller's device arrays out->i, out->j
  * (int32), out->k, out->rest (float32) of length `capacity`; out->n is set
  * to their number, which is ready to pass to pcloth_assemble / pcloth_step.
- * *found (may be NULL) receives the number of pairs found.  If more than
+ * *found (may be NULL) receives the number of pairs found (at most
+ * 2^31 - 1; the count itself is taken in 64 bits).  If more than
  * min(capacity, max_contacts) exist, nothing is written, out->n = 0 and
  * PCLOTH_ERR_CAPACITY is returned.  Cells have edge radius * (1 + 2^-7),
  * which finds every pair for coordinates within 2^15 cells of the origin.

@@ -198,7 +198,7 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   // contact finding hashes cells into a power-of-two table of at least 2n
   // buckets
   int64_t buckets = 1024;
-  while (buckets < 2 * n) buckets *= 2;
+  while (buckets < 2 * n && buckets < (int64_t(1) << 30)) buckets *= 2;
   h->hash_mask = uint32_t(buckets - 1);
   // scans run over the n + 1 per-row counts of the assembly, the n + 1
   // per-vertex pair counts and the buckets + 1 hash counts
@@ -266,7 +266,7 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->rowcnt, 2 * (n + 1)));
   A(dalloc(&h->newcnt, n + 1));
   A(dalloc(&h->newcol, ent2));
-  A(dalloc(&h->counters, 4));
+  A(dalloc(&h->counters, 8));
   A(dalloc(&h->hx, 3 * n));
   A(dalloc(&h->hv, 3 * n));
   A(dalloc(&h->hci, std::max<int64_t>(mc, 1)));

@@ -129,6 +129,7 @@ struct PairArgs {
   const int32_t* rowptr_s;
   const int32_t* colind_s;
   int32_t* count;          // count pass: partners of each vertex
+  unsigned long long* total;  // count pass: all partners, in 64 bits
   const int32_t* out_first;  // write pass: each vertex's first output slot
   int32_t* oi;
   int32_t* oj;
@@ -140,50 +141,64 @@ struct PairArgs {
 template <bool kWrite>
 __global__ void pair_pass(PairArgs a) {
   const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= a.n) return;
   const int32_t i = int32_t(t);
-  const float px = a.x[3 * t], py = a.x[3 * t + 1], pz = a.x[3 * t + 2];
-  const int32_t cx = cell_of(px, a.inv_edge), cy = cell_of(py, a.inv_edge);
-  const int32_t cz = cell_of(pz, a.inv_edge);
-  const int32_t base = kWrite ? a.out_first[i] : 0;
   int32_t c = 0;
-  for (int ox = -1; ox <= 1; ++ox) {
-    for (int oy = -1; oy <= 1; ++oy) {
-      for (int oz = -1; oz <= 1; ++oz) {
-        const int32_t nx = cx + ox, ny = cy + oy, nz = cz + oz;
-        const uint32_t b = cell_hash(nx, ny, nz, a.mask);
-        const int32_t u1 = a.first[b + 1];
-        for (int32_t u = a.first[b]; u < u1; ++u) {
-          const float4 s = a.slot[u];
-          const int32_t j = __float_as_int(s.w);
-          if (j <= i) continue;
-          if (cell_of(s.x, a.inv_edge) != nx || cell_of(s.y, a.inv_edge) != ny ||
-              cell_of(s.z, a.inv_edge) != nz)
-            continue;   // another cell with the same hash
-          const float dx = __fsub_rn(s.x, px);
-          const float dy = __fsub_rn(s.y, py);
-          const float dz = __fsub_rn(s.z, pz);
-          const float d2 = __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)),
-                                     __fmul_rn(dz, dz));
-          if (!(d2 < a.r2)) continue;
-          if (is_spring(a.rowptr_s, a.colind_s, i, j)) continue;
-          if (kWrite) a.oj[base + c] = j;
-          ++c;
+  int32_t base = 0;
+  if (t < a.n) {
+    const float px = a.x[3 * t], py = a.x[3 * t + 1], pz = a.x[3 * t + 2];
+    const int32_t cx = cell_of(px, a.inv_edge), cy = cell_of(py, a.inv_edge);
+    const int32_t cz = cell_of(pz, a.inv_edge);
+    if (kWrite) base = a.out_first[i];
+    for (int ox = -1; ox <= 1; ++ox) {
+      for (int oy = -1; oy <= 1; ++oy) {
+        for (int oz = -1; oz <= 1; ++oz) {
+          const int32_t nx = cx + ox, ny = cy + oy, nz = cz + oz;
+          const uint32_t b = cell_hash(nx, ny, nz, a.mask);
+          const int32_t u1 = a.first[b + 1];
+          for (int32_t u = a.first[b]; u < u1; ++u) {
+            const float4 s = a.slot[u];
+            const int32_t j = __float_as_int(s.w);
+            if (j <= i) continue;
+            if (cell_of(s.x, a.inv_edge) != nx || cell_of(s.y, a.inv_edge) != ny ||
+                cell_of(s.z, a.inv_edge) != nz)
+              continue;   // another cell with the same hash
+            const float dx = __fsub_rn(s.x, px);
+            const float dy = __fsub_rn(s.y, py);
+            const float dz = __fsub_rn(s.z, pz);
+            const float d2 = __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)),
+                                       __fmul_rn(dz, dz));
+            if (!(d2 < a.r2)) continue;
+            if (is_spring(a.rowptr_s, a.colind_s, i, j)) continue;
+            if (kWrite) a.oj[base + c] = j;
+            ++c;
+          }
         }
       }
     }
   }
-  if (!kWrite) {
-    a.count[i] = c;
-    if (i == a.n - 1) a.count[a.n] = 0;   // the scan's total slot
+  if (kWrite) {
+    if (t < a.n) {
+      sort_partners(a.oj + base, c);
+      for (int32_t q = 0; q < c; ++q) {
+        a.oi[base + q] = i;
+        a.ok[base + q] = a.k;
+        a.orest[base + q] = a.rest;
+      }
+    }
     return;
   }
-  sort_partners(a.oj + base, c);
-  for (int32_t q = 0; q < c; ++q) {
-    a.oi[base + q] = i;
-    a.ok[base + q] = a.k;
-    a.orest[base + q] = a.rest;
+  if (t < a.n) {
+    a.count[i] = c;
+    if (i == a.n - 1) a.count[a.n] = 0;   // the scan's total slot
   }
+  // The total in 64 bits (a warp's sum, then one atomic per warp): past 2^31
+  // pairs (a collapsed cloud) the int32 scan of the counts wraps, and the
+  // capacity test must still see the true number.  Every thread of the block
+  // gets here, so the warp is whole.
+  unsigned long long w = static_cast<unsigned long long>(c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) w += __shfl_down_sync(0xffffffffu, w, o);
+  if ((threadIdx.x & 31) == 0 && w != 0) atomicAdd(a.total, w);
 }
 
 }  // namespace
@@ -223,22 +238,26 @@ int find_contacts(Handle* h, const float* x, float radius, float stiffness,
   a.rowptr_s = h->rowptr_s;
   a.colind_s = h->colind_s;
   a.count = h->pair_first;
+  a.total = reinterpret_cast<unsigned long long*>(h->counters + 4);
+  e = cudaMemsetAsync(a.total, 0, sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "pair total reset");
   pair_pass<false><<<grid, 256, 0, s>>>(a);
   h->launches += 1;
   rc = check_launch(h, "pair count");
   if (rc != PCLOTH_OK) return rc;
   rc = scan_exclusive(h, h->pair_first, n + 1, h->counters + 2);
   if (rc != PCLOTH_OK) return rc;
-  int32_t total = 0;
-  e = cudaMemcpyAsync(&total, h->counters + 2, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  unsigned long long total64 = 0;
+  e = cudaMemcpyAsync(&total64, a.total, sizeof(total64), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(h, e, "pair count");
+  const int32_t total = int32_t(std::min<unsigned long long>(total64, INT32_MAX));
   if (found) *found = total;
   const int32_t cap = std::min<int32_t>(capacity, h->max_contacts);
-  if (total > cap) {
+  if (total64 > static_cast<unsigned long long>(cap)) {
     out->n = 0;
     return fail(h, PCLOTH_ERR_CAPACITY,
-                "found " + std::to_string(total) + " contacts, capacity " + std::to_string(cap));
+                "found " + std::to_string(total64) + " contacts, capacity " + std::to_string(cap));
   }
   if (total > 0) {
     a.out_first = h->pair_first;

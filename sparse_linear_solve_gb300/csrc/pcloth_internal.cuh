@@ -124,7 +124,8 @@ struct Handle {
                                    // entry of each row; then the scatter cursors
   int32_t* newcnt = nullptr;       // [n+1]: new blocks per row, scanned to those before it
   int32_t* newcol = nullptr;       // a row's new columns, at its first entry's index
-  int32_t* counters = nullptr;     // [0] = #new blocks, [1] = #valid entries, [2] pairs
+  int32_t* counters = nullptr;     // [0] = #new blocks, [1] = #valid entries, [2] scan totals
+                                   // of contact finding, [4..5] its pair count as uint64
 
   // host-input staging for pcloth_step_host
   float* hx = nullptr;

@@ -77,6 +77,24 @@ def test_contacts_capacity_and_empty():
     assert found == 0 and len(gi) == 0
 
 
+def test_contacts_count_past_int32():
+    """65,600 vertices at one point: 2,151,647,200 pairs, past 2^31 - 1 less
+    the springs.  The count must still exceed the capacity (not wrap), the
+    call must write nothing, and the reported count saturates at 2^31 - 1."""
+    w = W.tiny_cloth(n=8)
+    n = 65600
+    w.mass = np.concatenate([w.mass, np.full(n - w.n_verts, 1e-4, np.float32)])
+    w.n_verts = n
+    w.max_contacts = 100
+    pcl = pc.PCloth.from_workload(w, device=DEV)
+    x = np.zeros((n, 3), np.float32)
+    pairs = n * (n - 1) // 2 - len(w.spring_i)
+    assert pairs > 2**31 - 1
+    with pytest.raises(pc.PClothError) as ei:
+        pcl.find_contacts(to_dev(x), 1e-3, 1e3)
+    assert ei.value.code == pc.ERR_CAPACITY and ei.value.found == 2**31 - 1
+
+
 def test_found_contacts_drive_a_step_like_the_oracle():
     """The found list, fed to the step, gives the oracle's step with the
     oracle's own list."""
