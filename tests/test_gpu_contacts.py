@@ -77,6 +77,33 @@ def test_contacts_capacity_and_empty():
     assert found == 0 and len(gi) == 0
 
 
+def test_contacts_with_colliding_cells():
+    """Two of a vertex's 27 neighbour cells that share a bucket of the spatial
+    hash table (of 1,024 buckets for a cloud this small): the partner in one
+    of them must be found once, not once per cell that hashes to its bucket.
+    The cells were found by a search with the hash written out in numpy:
+    cells (1653, 1665, 1656) and (1654, 1666, 1658) share bucket 342 at
+    r = 3 mm."""
+    w = W.tiny_cloth(n=8)
+    r = np.float32(3e-3)
+    edge = np.float32(r * np.float32(1 + 1 / 128))
+    ca = np.array([1653, 1665, 1657], np.float32)
+    xa = ((ca + np.float32(0.5)) * edge).astype(np.float32)
+    xb = xa - np.array([0, 0, 0.6], np.float32) * edge   # in cell (1653, 1665, 1656)
+    inv = np.float32(1) / edge
+    assert np.array_equal(np.floor(xa * inv), ca)
+    assert np.array_equal(np.floor(xb * inv), ca - np.array([0, 0, 1], np.float32))
+    x = np.concatenate([w.x0, xa[None], xb[None]]).astype(np.float32)
+    w.mass = np.concatenate([w.mass, np.full(2, 1e-4, np.float32)])
+    w.n_verts = len(x)
+    w.max_contacts = 1000
+    pcl = pc.PCloth.from_workload(w, device=DEV)
+    oi, oj, total = oracle.find_contacts(x, float(r), springs_of(w))
+    gi, gj, gk, gr, found = gpu_pairs(pcl, x, float(r))
+    assert found == total and np.array_equal(gi, oi) and np.array_equal(gj, oj)
+    assert (w.n_verts - 2, w.n_verts - 1) in set(zip(gi.tolist(), gj.tolist()))
+
+
 def test_contacts_count_past_int32():
     """65,600 vertices at one point: 2,151,647,200 pairs, past 2^31 - 1 less
     the springs.  The count must still exceed the capacity (not wrap), the
