@@ -254,11 +254,10 @@ __device__ __forceinline__ float excess_sq(float3 v, float L0) {
 // block) and force F of one element seen from vertex i: K at x, force at
 // x~ = x + h v.  e = x_j - x_i (exact, see Edge), its length and the
 // advanced edge are shared by all elements of a block (BlockEdge, formed
-// once per block); each element costs two divisions.  Lengths come from
-// rsqrtf and the two quotients from __fdividef, each good to a few units in
-// the last place (~1e-7 relative): far inside the 1e-5 to which every block
-// is checked against the fp64 oracle, and the length excess, whose
-// cancellation is what needs care, is formed exactly beforehand.
+// once per block); each element costs two divisions.  The square roots and
+// divisions are the IEEE ones (correctly rounded): rsqrtf and __fdividef,
+// good to a few units in the last place, made the assembly 4% faster and
+// are left out so that every operation of the element terms is IEEE.
 //
 // K = a I + c d d^T with a = k max(0, 1 - L0/l), c = k - a.  The length
 // excess l - L0 is formed as (|e|^2 - L0^2) / (l + L0) with the squares in
@@ -297,14 +296,12 @@ __device__ __forceinline__ BlockEdge block_edge(float3 xi, float3 xj, float3 vi,
   const float3 h = b.e.hi, o = b.e.lo;
   b.l2 = fmaf(h.x, h.x, fmaf(h.y, h.y, h.z * h.z)) +
          2.0f * fmaf(h.x, o.x, fmaf(h.y, o.y, h.z * o.z));
-  const float rl = rsqrtf(b.l2);
-  b.l = b.l2 * rl;
-  b.inv_l2 = rl * rl;
+  b.l = sqrtf(b.l2);
+  b.inv_l2 = 1.0f / b.l2;
   const float3 w = make_float3(vj.x - vi.x, vj.y - vi.y, vj.z - vi.z);
   b.adv = make_float3(fmaf(dt, w.x, h.x) + o.x, fmaf(dt, w.y, h.y) + o.y,
                       fmaf(dt, w.z, h.z) + o.z);
-  const float lt2 = b.adv.x * b.adv.x + b.adv.y * b.adv.y + b.adv.z * b.adv.z;
-  b.lt = lt2 * rsqrtf(lt2);
+  b.lt = sqrtf(b.adv.x * b.adv.x + b.adv.y * b.adv.y + b.adv.z * b.adv.z);
   return b;
 }
 
@@ -313,7 +310,7 @@ __device__ __forceinline__ void element_terms(const BlockEdge& b, float h2, floa
   const float3 h = b.e.hi, o = b.e.lo;
   const float l = b.l;
   // max(0, 1 - L0/l) = max(0, (l - L0) / l), with l - L0 = (|e|^2 - L0^2) / (l + L0)
-  const float tension = fmaxf(0.0f, __fdividef(excess_sq(h, o, L0), (l + L0) * l));
+  const float tension = fmaxf(0.0f, excess_sq(h, o, L0) / ((l + L0) * l));
   const float a = k * tension;
   const float c = k - a;
   const float A = -h2 * a;
@@ -325,7 +322,7 @@ __device__ __forceinline__ void element_terms(const BlockEdge& b, float h2, floa
   K[4] += scaled_entry(S, h.y, o.y, h.z, o.z);
   K[5] += scaled_entry(S, h.z, o.z, h.z, o.z) + A;
   // force at the advanced positions: k (l~ - L0) / l~ along the advanced edge
-  const float s = k * __fdividef(excess_sq(b.adv, L0), (b.lt + L0) * b.lt);
+  const float s = k * excess_sq(b.adv, L0) / ((b.lt + L0) * b.lt);
   F[0] += s * b.adv.x;
   F[1] += s * b.adv.y;
   F[2] += s * b.adv.z;
@@ -429,14 +426,12 @@ __device__ __forceinline__ void finish_row(const AsmArgs& a, int32_t i, int64_t 
 // 0.47 ms, 1 lane 0.62 ms; four or more CTAs per SM spill and lose.  Fewer
 // lanes cut the butterfly's and the row finish's share of the
 // instructions; one lane per row leaves each row's loads in a serial chain.
-// On that cloth the kernel then took 380 us (ncu); rsqrtf and __fdividef for
-// the IEEE square roots and divisions, the block stores as one 16- and one
-// 8-byte word, and the diagonal taken out of the lanes' loop brought it to
-// 276 us (the whole assembly 0.45 -> 0.345 ms per step).  Contacts cost
-// the most per element: without them the assembly took 0.20 ms.  One
-// element loop for springs and contacts, and cursors in place of a
-// merge-path search per block and a search of the contact run, brought
-// the whole assembly to 0.30 ms.
+// On that cloth the kernel then took 380 us (ncu); the block stores as one
+// 16- and one 8-byte word and the diagonal taken out of the lanes' loop cut
+// it most.  Contacts cost the most per element: without them the assembly
+// takes 0.20 ms.  One element loop for springs and contacts, and cursors in
+// place of a merge-path search per block and a search of the contact run,
+// brought the whole assembly from 0.45 to 0.305 ms per step.
 #ifndef PCLOTH_ASM_CTAS
 #define PCLOTH_ASM_CTAS 3
 #endif
