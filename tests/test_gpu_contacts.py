@@ -77,6 +77,26 @@ def test_contacts_capacity_and_empty():
     assert found == 0 and len(gi) == 0
 
 
+def test_contacts_at_exactly_the_capacity():
+    """As many pairs as the capacity allows: all are written; one more pair
+    than the capacity: nothing is written and the count is reported."""
+    w = W.tiny_cloth(n=24)
+    n = 3000
+    x = cloud(n, 0.05, 11, clusters=4)
+    x[: w.n_verts] = w.x0
+    w.mass = np.concatenate([w.mass, np.full(n - w.n_verts, 1e-4, np.float32)])
+    w.n_verts = n
+    w.max_contacts = 200000
+    pcl = pc.PCloth.from_workload(w, device=DEV)
+    oi, oj, total = oracle.find_contacts(x, 3e-3, springs_of(w))
+    assert total > 1
+    gi, gj, _, _, found = gpu_pairs(pcl, x, 3e-3, capacity=total)
+    assert found == total and np.array_equal(gi, oi) and np.array_equal(gj, oj)
+    with pytest.raises(pc.PClothError) as ei:
+        pcl.find_contacts(to_dev(x), 3e-3, 1e3, total - 1)
+    assert ei.value.code == pc.ERR_CAPACITY and ei.value.found == total
+
+
 def test_contacts_with_colliding_cells():
     """Two of a vertex's 27 neighbour cells that share a bucket of the spatial
     hash table (of 1,024 buckets for a cloud this small): the partner in one
