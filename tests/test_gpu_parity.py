@@ -240,6 +240,46 @@ def test_deterministic_bitwise():
         assert np.array_equal(np.asarray(a), np.asarray(b))
 
 
+@pytest.mark.parametrize("make_w", [lambda: W.folded_stack(n=29, steps=2),
+                                    lambda: W.jittered_cloth(n=48),
+                                    lambda: W.tiny_cloth(rest_from_grid=True)],
+                         ids=["folded4x29", "jitter48", "tiny32_tension"])
+def test_blocks_bitwise_symmetric_and_rows_sum_to_the_mass(make_w):
+    """Two properties of Eq. (3)'s matrix that the assembly keeps exactly.
+    A_ji = A_ij^T = A_ij: the block (j, i) is computed from the negated edge
+    and must carry the bits of the block (i, j).  And the rows of A sum to
+    M (every element stiffness is subtracted from the diagonal it adds to):
+    the diagonal is formed from the row's stored off-diagonal blocks with a
+    compensated sum, so sum_j A_ij - m_i I, taken in fp64 from the stored
+    fp32 blocks, stays within the rounding of the diagonal entry (2 ulp) plus
+    the compensated sum's own second-order error (2^-40 of the row's sum of
+    magnitudes; a plain fp32 sum would leave about 2^-24 of it)."""
+    w = make_w()
+    c = w.contacts(1)
+    pcl = make(w)
+    pcl.assemble(to_dev(w.x0), to_dev(w.v0), c if c.n else None, w.h)
+    g = pcl.export()
+    rowptr = g["rowptr"].cpu().numpy().astype(np.int64)
+    colind = g["colind"].cpu().numpy()
+    vals = g["vals"].cpu().numpy()
+    n = w.n_verts
+    rows = np.repeat(np.arange(n), np.diff(rowptr))
+    where = {(int(i), int(j)): q for q, (i, j) in enumerate(zip(rows, colind))}
+    mirror = np.array([where[(int(j), int(i))] for i, j in zip(rows, colind)])
+    bits = vals.view(np.uint32)
+    assert np.array_equal(bits, bits[mirror]), "A_ij and A_ji differ in their bits"
+    assert np.array_equal(bits, np.transpose(bits, (0, 2, 1))), "a block is not symmetric"
+    sums = np.zeros((n, 3, 3))
+    np.add.at(sums, rows, vals.astype(np.float64))
+    resid = sums - w.mass.astype(np.float64)[:, None, None] * np.eye(3)
+    absum = np.zeros((n, 3, 3))
+    np.add.at(absum, rows, np.abs(vals.astype(np.float64)))
+    diag = vals[rows == colind].astype(np.float64)
+    ulp = np.spacing(np.abs(diag).astype(np.float32)).astype(np.float64)
+    tol = 2.0 * ulp + 2.0**-40 * absum
+    assert np.all(np.abs(resid) <= tol), float(np.max(np.abs(resid) / tol))
+
+
 def test_zero_stiffness_one_iteration():
     w = W.tiny_cloth(n=12)
     w.spring_k[:] = 0.0
