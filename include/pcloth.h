@@ -138,8 +138,9 @@ int pcloth_spmv(pcloth_t h, const float* in, float* out);
  * *found (may be NULL) receives the number of pairs found (at most
  * 2^31 - 1; the count itself is taken in 64 bits).  If more than
  * min(capacity, max_contacts) exist, nothing is written, out->n = 0 and
- * PCLOTH_ERR_CAPACITY is returned.  Cells have edge radius * (1 + 2^-7),
- * which finds every pair for coordinates within 2^15 cells of the origin.
+ * PCLOTH_ERR_CAPACITY is returned.  Cells have edge 2 radius (1 + 2^-7) and
+ * each vertex searches the 8 cells that can hold a partner, which finds
+ * every pair for coordinates within 2^14 cells of the origin.
  * Synchronises. */
 int pcloth_find_contacts(pcloth_t h, const float* x, float radius, float stiffness,
                          pcloth_springs* out, int32_t capacity, int32_t* found);

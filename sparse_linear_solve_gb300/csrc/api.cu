@@ -34,7 +34,7 @@ void free_handle(Handle* h) {
   cudaStreamSynchronize(h->stream);
   void* bufs[] = {h->mass, h->rowptr_s, h->colind_s, h->sblk_ptr, h->sentry,
                   h->rowptr, h->colind, h->vals, h->rhs, h->vec_arena,
-                  h->centry, h->hash_first, h->hash_where, h->hash_slot, h->pair_first,
+                  h->centry, h->hash_first, h->hash_where, h->hash_slot, h->hash_range, h->pair_first,
                   h->scan_tmp, h->rowcnt, h->newcnt, h->newcol,
                   h->counters,
                   h->hx, h->hv, h->hci, h->hcj, h->hck, h->hcr,
@@ -261,6 +261,7 @@ int pcloth_create(const pcloth_mesh* mesh, const pcloth_springs* sp,
   A(dalloc(&h->hash_first, buckets + 1));
   A(dalloc(&h->hash_where, n));
   A(dalloc(&h->hash_slot, n));
+  A(dalloc(&h->hash_range, buckets));
   A(dalloc(&h->pair_first, n + 1));
   A(dalloc(&h->scan_tmp, scan_tiles + 1));
   A(dalloc(&h->rowcnt, 2 * (n + 1)));

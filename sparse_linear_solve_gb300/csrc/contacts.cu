@@ -5,22 +5,25 @@
 // a radius r that is not a spring becomes a contact (a spring of stiffness
 // k_c and rest length r), listed in (i, j) order.
 //
-//   hash_count    each vertex to its cell of edge r (1 + 2^-7): the slight
-//                 enlargement keeps every pair closer than r in neighbouring
-//                 cells despite the rounding of x / edge, for coordinates up
-//                 to 2^15 cells from the origin (65 m at r = 2 mm); the cell
-//                 to a bucket of a table of T >= 2n buckets by the hash of
+//   hash_count    each vertex to its cell of edge 2r (1 + 2^-7); the cell to
+//                 a bucket of a table of T >= 2n buckets by the hash of
 //                 Teschner et al. (2003, "Optimized Spatial Hashing for
 //                 Collision Detection of Deformable Objects"), counted with
 //                 an atomic that also gives the vertex its place in the bucket
 //   scan          the buckets' first slots
 //   hash_fill     each vertex's position and index into its bucket's slot
-//   pair_pass     per vertex i, twice: the 27 buckets of the cells around
-//                 its own; a candidate j > i counts if it lies in that very
-//                 cell (buckets are shared by colliding cells), passes the
-//                 exact float32 test ((dx dx + dy dy) + dz dz < r r, each
-//                 operation rounded) and is no spring (a binary search in
-//                 the static pattern).  The first pass counts, a scan gives
+//   hash_ranges   each bucket's slot range as one 8-byte word
+//   pair_pass     per vertex i, twice: the 8 cells that can hold a partner
+//                 -- per axis its own cell and the next one on the side of
+//                 the half of the cell that holds the vertex, as a partner
+//                 is less than half a cell away.  The enlargement 1 + 2^-7
+//                 keeps that true despite the rounding of x / edge, for
+//                 coordinates up to 2^14 cells from the origin (65 m at
+//                 r = 2 mm).  A candidate j > i counts if it lies in the
+//                 searched cell (buckets are shared by colliding cells),
+//                 passes the exact float32 test ((dx dx + dy dy) + dz dz <
+//                 r r, each operation rounded) and is no spring (a binary
+//                 search in the static pattern).  The first pass counts, a scan gives
 //                 every vertex its first output slot, and the second pass
 //                 writes the partners and sorts them, so the list comes out
 //                 in (i, j) order whatever the order inside the buckets.
@@ -68,6 +71,13 @@ __global__ void hash_fill(int32_t n, const float* __restrict__ x, const int2* __
   if (i >= n) return;
   const int2 w = where[i];
   slot[first[w.x] + w.y] = make_float4(x[3 * i], x[3 * i + 1], x[3 * i + 2], __int_as_float(int32_t(i)));
+}
+
+// Each bucket's slot range as one 8-byte word, so that a lookup is one load.
+__global__ void hash_ranges(int32_t nb, const int32_t* __restrict__ first,
+                            int2* __restrict__ range) {
+  const int64_t b = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (b < nb) range[b] = make_int2(first[b], first[b + 1]);
 }
 
 __device__ __forceinline__ bool is_spring(const int32_t* __restrict__ rowptr_s,
@@ -124,7 +134,7 @@ struct PairArgs {
   float r2, inv_edge;
   uint32_t mask;
   const float* x;
-  const int32_t* first;    // [T + 1] first slot of each bucket
+  const int2* range;       // [T] first and end slot of each bucket
   const float4* slot;      // [n] (x, y, z, index) in bucket order
   const int32_t* rowptr_s;
   const int32_t* colind_s;
@@ -148,14 +158,20 @@ __global__ void pair_pass(PairArgs a) {
     const float px = a.x[3 * t], py = a.x[3 * t + 1], pz = a.x[3 * t + 2];
     const int32_t cx = cell_of(px, a.inv_edge), cy = cell_of(py, a.inv_edge);
     const int32_t cz = cell_of(pz, a.inv_edge);
+    // cells of edge 2r: the partners lie in this cell or the next one on
+    // the side of the half of the cell that holds the vertex, per axis
+    const float tx = px * a.inv_edge, ty = py * a.inv_edge, tz = pz * a.inv_edge;
+    const int sx = (tx - floorf(tx) >= 0.5f) ? 1 : -1;
+    const int sy = (ty - floorf(ty) >= 0.5f) ? 1 : -1;
+    const int sz = (tz - floorf(tz) >= 0.5f) ? 1 : -1;
     if (kWrite) base = a.out_first[i];
-    for (int ox = -1; ox <= 1; ++ox) {
-      for (int oy = -1; oy <= 1; ++oy) {
-        for (int oz = -1; oz <= 1; ++oz) {
-          const int32_t nx = cx + ox, ny = cy + oy, nz = cz + oz;
+    for (int ox = 0; ox <= 1; ++ox) {
+      for (int oy = 0; oy <= 1; ++oy) {
+        for (int oz = 0; oz <= 1; ++oz) {
+          const int32_t nx = cx + ox * sx, ny = cy + oy * sy, nz = cz + oz * sz;
           const uint32_t b = cell_hash(nx, ny, nz, a.mask);
-          const int32_t u1 = a.first[b + 1];
-          for (int32_t u = a.first[b]; u < u1; ++u) {
+          const int2 rg = a.range[b];
+          for (int32_t u = rg.x; u < rg.y; ++u) {
             const float4 s = a.slot[u];
             const int32_t j = __float_as_int(s.w);
             if (j <= i) continue;
@@ -207,7 +223,7 @@ int find_contacts(Handle* h, const float* x, float radius, float stiffness,
                   pcloth_springs* out, int32_t capacity, int32_t* found) {
   cudaStream_t s = h->stream;
   const int32_t n = h->n;
-  const float edge = radius * (1.0f + 1.0f / 128.0f);
+  const float edge = 2.0f * radius * (1.0f + 1.0f / 128.0f);
   const float inv_edge = 1.0f / edge;
   const float r2 = radius * radius;   // float32, as the test compares
   const int32_t nb = int32_t(h->hash_mask) + 1;   // buckets
@@ -223,7 +239,8 @@ int find_contacts(Handle* h, const float* x, float radius, float stiffness,
   rc = scan_exclusive(h, h->hash_first, nb + 1, h->counters + 2);
   if (rc != PCLOTH_OK) return rc;
   hash_fill<<<grid, 256, 0, s>>>(n, x, h->hash_where, h->hash_first, h->hash_slot);
-  h->launches += 1;
+  hash_ranges<<<(nb + 255) / 256, 256, 0, s>>>(nb, h->hash_first, h->hash_range);
+  h->launches += 2;
   rc = check_launch(h, "hash fill");
   if (rc != PCLOTH_OK) return rc;
   // partners per vertex, their scan, and the total on the host
@@ -233,7 +250,7 @@ int find_contacts(Handle* h, const float* x, float radius, float stiffness,
   a.inv_edge = inv_edge;
   a.mask = h->hash_mask;
   a.x = x;
-  a.first = h->hash_first;
+  a.range = h->hash_range;
   a.slot = h->hash_slot;
   a.rowptr_s = h->rowptr_s;
   a.colind_s = h->colind_s;

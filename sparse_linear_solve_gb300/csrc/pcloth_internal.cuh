@@ -162,6 +162,7 @@ struct Handle {
   int32_t* hash_first = nullptr;   // [buckets + 1]: counts, scanned to each bucket's first slot
   int2* hash_where = nullptr;      // [n]: each vertex's bucket and place in it
   float4* hash_slot = nullptr;     // [n]: (x, y, z, index) in bucket order
+  int2* hash_range = nullptr;      // [buckets]: each bucket's first and end slot
   int32_t* pair_first = nullptr;   // [n + 1]: partners per vertex, scanned to first output
 
   // block-ELL copy of the assembled matrix (the pages' layout), built on

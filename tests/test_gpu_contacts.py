@@ -98,21 +98,22 @@ def test_contacts_at_exactly_the_capacity():
 
 
 def test_contacts_with_colliding_cells():
-    """Two of a vertex's 27 neighbour cells that share a bucket of the spatial
+    """Two of the cells a vertex searches that share a bucket of the spatial
     hash table (of 1,024 buckets for a cloud this small): the partner in one
     of them must be found once, not once per cell that hashes to its bucket.
-    The cells were found by a search with the hash written out in numpy:
-    cells (1653, 1665, 1656) and (1654, 1666, 1658) share bucket 342 at
-    r = 3 mm."""
+    Cells have edge 2 r (1 + 2^-7); a vertex a quarter of the way into its
+    cell searches it and the cells below it.  The cells were found by a
+    search with the hash written out in numpy: at r = 3 mm the searched
+    cells (828, 826, 826) and (827, 827, 826) share bucket 444."""
     w = W.tiny_cloth(n=8)
     r = np.float32(3e-3)
-    edge = np.float32(r * np.float32(1 + 1 / 128))
-    ca = np.array([1653, 1665, 1657], np.float32)
-    xa = ((ca + np.float32(0.5)) * edge).astype(np.float32)
-    xb = xa - np.array([0, 0, 0.6], np.float32) * edge   # in cell (1653, 1665, 1656)
+    edge = np.float32(np.float32(2) * r * np.float32(1 + 1 / 128))
+    ca = np.array([828, 827, 826], np.float32)
+    xa = ((ca + np.float32(0.25)) * edge).astype(np.float32)
+    xb = xa - np.array([0, 0.3, 0], np.float32) * edge   # in cell (828, 826, 826)
     inv = np.float32(1) / edge
     assert np.array_equal(np.floor(xa * inv), ca)
-    assert np.array_equal(np.floor(xb * inv), ca - np.array([0, 0, 1], np.float32))
+    assert np.array_equal(np.floor(xb * inv), ca - np.array([0, 1, 0], np.float32))
     x = np.concatenate([w.x0, xa[None], xb[None]]).astype(np.float32)
     w.mass = np.concatenate([w.mass, np.full(2, 1e-4, np.float32)])
     w.n_verts = len(x)
